@@ -1,0 +1,248 @@
+"""ctypes front end of the fp64 oracle in ``ring_oracle.c``.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).  Arrays are numpy
+float64, C-contiguous, shaped [B, H, S, d] (rows [B, H, S]).  The C code is
+compiled on first use with the system ``gcc`` (OpenMP over rows / heads).
+
+Besides the attention routines, this module holds the analytic helpers the
+pages print numbers for (the "Context Parallelism" guide, section 2,
+"Communication" and "Worked Example"):
+
+* bytes rotated per ring step: K and V of one chunk, 2 * (S/P) * d_k * 2 bytes
+  for BF16 -- per head; the worked example's 32K x 128 x 2 bytes x 2 = 16 MB;
+* total over the P - 1 rotations, (P - 1) * 2 * (S/P) * d_k * 2 bytes
+  (the example's 3 steps = 48 MB);
+* KV-cache bytes per token of a multi-head model: 2 (K and V) * layers *
+  heads * d_k * bytes -- 512 KB/token for the 7B / 32-head / d_k = 128 example
+  at 32 layers and 2 bytes (guide section 1 and the worked example);
+* score-matrix elements S^2 (guide section 1: 128K^2 = 16 billion).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+KIND_LOCAL = 0
+KIND_FULL = 1
+KIND_SKIP = 2
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ring_oracle.c")
+_LIB = os.path.join(_HERE, "libringoracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build_oracle(force: bool = False) -> str:
+    """Compile ``ring_oracle.c`` into ``libringoracle.so`` (plain C, -O2, OpenMP)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
+               "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build_oracle())
+        dp = ctypes.POINTER(ctypes.c_double)
+        ip = ctypes.POINTER(ctypes.c_int)
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        c_int, c_long, c_double = ctypes.c_int, ctypes.c_long, ctypes.c_double
+        lib.oracle_ring_visits.argtypes = [c_int, c_int, c_int, ip, ip]
+        lib.oracle_ring_visits.restype = c_int
+        lib.oracle_naive_fwd.argtypes = [dp, dp, dp, c_int, c_int, c_int, c_int,
+                                         c_int, c_double, dp, dp]
+        lib.oracle_naive_fwd.restype = None
+        lib.oracle_naive_fwd_rows.argtypes = [dp, dp, dp, c_int, c_int, c_int,
+                                              c_int, c_int, c_double, i64p,
+                                              c_long, dp, dp]
+        lib.oracle_naive_fwd_rows.restype = None
+        lib.oracle_merge.argtypes = [dp, dp, dp, dp, c_long, c_int, dp, dp]
+        lib.oracle_merge.restype = None
+        lib.oracle_ring_fwd.argtypes = [dp, dp, dp, c_int, c_int, c_int, c_int,
+                                        c_int, c_int, c_double, dp, dp, ip]
+        lib.oracle_ring_fwd.restype = c_int
+        lib.oracle_bwd.argtypes = [dp, dp, dp, dp, c_int, c_int, c_int, c_int,
+                                   c_int, c_double, dp, dp, dp, dp, dp]
+        lib.oracle_bwd.restype = None
+        lib.oracle_bwd_dq_rows.argtypes = [dp, dp, dp, dp, c_int, c_int, c_int,
+                                           c_int, c_int, c_double, i64p, c_long,
+                                           dp, dp]
+        lib.oracle_bwd_dq_rows.restype = None
+        lib.oracle_partial.argtypes = [dp, c_long, c_long, dp, dp, c_long, c_long,
+                                       c_int, c_int, c_double, dp, dp]
+        lib.oracle_partial.restype = None
+        _lib = lib
+        return lib
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray, ty=ctypes.c_double):
+    return a.ctypes.data_as(ctypes.POINTER(ty))
+
+
+def _shape4(q):
+    if q.ndim != 4:
+        raise ValueError("expected [B, H, S, d]")
+    return q.shape
+
+
+def ring_visits(P: int, causal: bool, i: int):
+    """Visit list of query chunk i: list of (t, j, kind) for t = 0..P-1."""
+    lib = _load()
+    js = (ctypes.c_int * P)()
+    ks = (ctypes.c_int * P)()
+    n = lib.oracle_ring_visits(P, int(bool(causal)), i, js, ks)
+    if n < 0:
+        raise ValueError("bad ring arguments")
+    return [(t, js[t], ks[t]) for t in range(P)]
+
+
+def naive_fwd(q, k, v, causal: bool, scale: float):
+    """Definition over whole rows -> (O [B,H,S,d], LSE [B,H,S]) in fp64."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, S, d = _shape4(q)
+    o = np.empty_like(q)
+    lse = np.empty((B, H, S), dtype=np.float64)
+    _load().oracle_naive_fwd(_ptr(q), _ptr(k), _ptr(v), B, H, S, d,
+                             int(bool(causal)), float(scale), _ptr(o), _ptr(lse))
+    return o, lse
+
+
+def naive_fwd_rows(q, k, v, causal: bool, scale: float, rows):
+    """Definition for selected flat rows (index bh * S + r) -> (O [n,d], LSE [n])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, S, d = _shape4(q)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    if rows.size and (rows.min() < 0 or rows.max() >= B * H * S):
+        raise ValueError("row index out of range")
+    o = np.empty((rows.size, d), dtype=np.float64)
+    lse = np.empty(rows.size, dtype=np.float64)
+    _load().oracle_naive_fwd_rows(_ptr(q), _ptr(k), _ptr(v), B, H, S, d,
+                                  int(bool(causal)), float(scale),
+                                  _ptr(rows, ctypes.c_int64), rows.size,
+                                  _ptr(o), _ptr(lse))
+    return o, lse
+
+
+def merge(o_a, lse_a, o_b, lse_b):
+    """Log-sum-exp merge of two partials, row-wise -> (O, LSE)."""
+    o_a, o_b = _f64(o_a), _f64(o_b)
+    lse_a, lse_b = _f64(lse_a), _f64(lse_b)
+    if o_a.shape != o_b.shape or lse_a.shape != lse_b.shape:
+        raise ValueError("shape mismatch")
+    d = o_a.shape[-1]
+    rows = lse_a.size
+    if o_a.size != rows * d:
+        raise ValueError("O and LSE disagree")
+    o = np.empty_like(o_a)
+    lse = np.empty_like(lse_a)
+    _load().oracle_merge(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), rows, d,
+                         _ptr(o), _ptr(lse))
+    return o, lse
+
+
+def ring_fwd(q, k, v, P: int, causal: bool, scale: float):
+    """Ring schedule taken literally -> (O, LSE, visit_log [P, P, 3])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, S, d = _shape4(q)
+    o = np.empty_like(q)
+    lse = np.empty((B, H, S), dtype=np.float64)
+    log = np.zeros((P, P, 3), dtype=np.int32)
+    rc = _load().oracle_ring_fwd(_ptr(q), _ptr(k), _ptr(v), B, H, S, d, P,
+                                 int(bool(causal)), float(scale), _ptr(o), _ptr(lse),
+                                 _ptr(log, ctypes.c_int))
+    if rc != 0:
+        raise ValueError("bad ring arguments (S must divide into P equal chunks)")
+    return o, lse, log
+
+
+def partial(q_rows, r0: int, k_rows, v_rows, c0: int, causal: bool, scale: float):
+    """One ring step's partial: query rows at global positions r0.. against
+    keys at c0.. (one head, [n, d] each) -> (O [nq, d], LSE [nq])."""
+    q_rows, k_rows, v_rows = _f64(q_rows), _f64(k_rows), _f64(v_rows)
+    nq, d = q_rows.shape
+    nk = k_rows.shape[0]
+    if k_rows.shape != (nk, d) or v_rows.shape != (nk, d):
+        raise ValueError("shape mismatch")
+    o = np.empty((nq, d), dtype=np.float64)
+    lse = np.empty(nq, dtype=np.float64)
+    _load().oracle_partial(_ptr(q_rows), r0, nq, _ptr(k_rows), _ptr(v_rows), c0, nk, d,
+                           int(bool(causal)), float(scale), _ptr(o), _ptr(lse))
+    return o, lse
+
+
+def bwd(q, k, v, dO, causal: bool, scale: float):
+    """Plain derivative of L = sum(dO * O) -> (dQ, dK, dV, LSE, D)."""
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    B, H, S, d = _shape4(q)
+    dq = np.empty_like(q)
+    dk = np.empty_like(q)
+    dv = np.empty_like(q)
+    lse = np.empty((B, H, S), dtype=np.float64)
+    D = np.empty((B, H, S), dtype=np.float64)
+    _load().oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), B, H, S, d,
+                       int(bool(causal)), float(scale), _ptr(dq), _ptr(dk), _ptr(dv),
+                       _ptr(lse), _ptr(D))
+    return dq, dk, dv, lse, D
+
+
+def bwd_dq_rows(q, k, v, dO, causal: bool, scale: float, rows):
+    """dQ and D for selected flat query rows -> (dQ [n,d], D [n])."""
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    B, H, S, d = _shape4(q)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    if rows.size and (rows.min() < 0 or rows.max() >= B * H * S):
+        raise ValueError("row index out of range")
+    dq = np.empty((rows.size, d), dtype=np.float64)
+    D = np.empty(rows.size, dtype=np.float64)
+    _load().oracle_bwd_dq_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), B, H, S, d,
+                               int(bool(causal)), float(scale),
+                               _ptr(rows, ctypes.c_int64), rows.size, _ptr(dq), _ptr(D))
+    return dq, D
+
+
+# ---------------------------------------------------------------------------
+# Analytic helpers ("Context Parallelism" guide, section 2)
+# ---------------------------------------------------------------------------
+
+def ring_step_bytes(S: int, P: int, d_k: int, elem_bytes: int = 2, heads: int = 1) -> int:
+    """K and V of one chunk: 2 * (S/P) * d_k * elem_bytes per head."""
+    if S % P:
+        raise ValueError("S must divide into P chunks")
+    return 2 * (S // P) * d_k * elem_bytes * heads
+
+
+def ring_total_bytes(S: int, P: int, d_k: int, elem_bytes: int = 2, heads: int = 1) -> int:
+    """All P - 1 rotations: (P - 1) * 2 * (S/P) * d_k * elem_bytes per head."""
+    return (P - 1) * ring_step_bytes(S, P, d_k, elem_bytes, heads)
+
+
+def kv_cache_bytes_per_token(layers: int, heads: int, d_k: int, elem_bytes: int = 2) -> int:
+    """K and V of every layer and head for one token."""
+    return 2 * layers * heads * d_k * elem_bytes
+
+
+def score_matrix_elements(S: int) -> int:
+    """Entries of one head's S x S score matrix."""
+    return S * S
+
+
+def attention_flops(B: int, H: int, S: int, d: int, causal: bool) -> int:
+    """Forward FLOPs counted as 4 d per allowed (query, key) pair (QK^T and
+    PV, one multiply-add = 2 FLOPs each).  Causal counts pairs c <= r."""
+    pairs = S * (S + 1) // 2 if causal else S * S
+    return 4 * d * pairs * B * H
