@@ -1,0 +1,394 @@
+#!/usr/bin/env python3
+"""Throughput of exact ring attention (forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+One step is one pass of the whole hot path over one batch of synthetic
+input: ring_attn_fwd (O, LSE) followed by ring_attn_bwd (dQ, dK, dV; the
+backward runs its preparation, main and dQ-conversion kernels).  The default
+workload is the 128K causal forward + backward shape: B=1, H=32, S=131072,
+d=128, P=4 chunks of 32768, bf16, N(0,1) inputs (seeded, generated on the
+device).  FLOPs are counted as 4 d per allowed (query, key) pair for the
+forward (causal pairs only) and 2.5x that for the backward.
+
+The JSON line carries: whole-job TFLOP/s over all ranks (``value``), tokens/s,
+per-pass times, the roofline of the dominant kernel (timed with CUDA events on
+its launch stream inside the timed region), the end-to-end number with host
+buffers (pinned host -> device copies of q, k, v, dO and device -> host copies
+of O, LSE, dQ, dK, dV inside the timed region), the SM clocks sampled during
+the timed region, and the CPU oracle timed on a bounded sample.
+
+``--impl reference`` times the fp64 CPU oracle (the only reference this
+method has) on the same workload, metric and unit, each step a bounded sample
+of rows.  Under torchrun (N > 1) every rank runs its own replica of the
+workload on its own GPU (weak scaling; no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "attention TFLOP/s and tokens/s at 1 GB300 (fwd, fwd+bwd); % of dense BF16 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=workloads.FWDBWD_CAUSAL_128K.name,
+                    choices=[w.name for w in workloads.ALL])
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def pair_count(S: int, causal: bool) -> int:
+    return S * (S + 1) // 2 if causal else S * S
+
+
+def flops(w, B, H, S, d, causal):
+    fwd = 4 * d * pair_count(S, causal) * B * H
+    bwd = 5 * fwd // 2 if w.backward else 0
+    return fwd, bwd
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        self.bus = None
+        try:
+            props = torch.cuda.get_device_properties(device_index)
+            bus = getattr(props, "pci_bus_id", None)
+            if bus is None:
+                bus = getattr(props, "pci_bus_id_str", None)
+            self.bus = str(bus).lower() if bus is not None else None
+        except Exception:
+            self.bus = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        if self.bus:
+            mine = [r for r in rows if r[1].lower().endswith(self.bus[-12:])]
+            rows = mine or rows
+        if rows:
+            first_index = rows[0][0]
+            rows = [r for r in rows if r[0] == first_index]
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            for name, val in zip(names, r[6:10]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline only)
+# ---------------------------------------------------------------------------
+def oracle_sample(w, inp, seconds: float):
+    """Time the fp64 oracle on sampled rows of head 0: forward (O, LSE) plus
+    the dQ part of the backward for each sampled row.  Returns the measured
+    FLOP rate in TFLOP/s (counted as 4 d per pair forward + 6 d per pair for
+    the backward's P, dP and dQ products of that row), cores, sample text."""
+    import numpy as np
+
+    import oracle
+    oracle.build_oracle()
+    S, d, causal, sc = inp["S"], inp["d"], inp["causal"], inp["scale"]
+    head = [inp[x][0:1, 0:1].to("cpu", torch.float64).numpy() for x in ("q", "k", "v")]
+    do = (inp["do"][0:1, 0:1].to("cpu", torch.float64).numpy() if w.backward else None)
+    g = np.random.default_rng(1234)
+    rows_done, flop, t_used = 0, 0.0, 0.0
+    batch = 8
+    while t_used < seconds and rows_done < S:
+        rows = np.sort(g.integers(0, S, batch))
+        t0 = time.perf_counter()
+        oracle.naive_fwd_rows(*head, causal, sc, rows)
+        if do is not None:
+            oracle.bwd_dq_rows(*head, do, causal, sc, rows)
+        t_used += time.perf_counter() - t0
+        pairs = (rows + 1).sum() if causal else S * len(rows)
+        flop += float(pairs) * d * (4 + (6 if do is not None else 0))
+        rows_done += len(rows)
+        batch = min(256, batch * 2)
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    sample = (f"{rows_done} random query rows of head 0 (S={S}, d={d}, "
+              f"{'causal' if causal else 'full'}): oracle forward"
+              + (" + dQ-row backward" if do is not None else "") +
+              f", {t_used:.1f} s; rate scaled to the workload's FLOP count")
+    return flop / t_used / 1e12, cores, sample, t_used
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args, w):
+    """The oracle timed as it stands on the host cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    inp = workloads.make(w, device="cpu", keep_fp32=False, S=None)
+    B, H, S, d = inp["B"], inp["H"], inp["S"], inp["d"]
+    f_fwd, f_bwd = flops(w, B, H, S, d, inp["causal"])
+    total = f_fwd + f_bwd
+    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    rates = []
+    for i in range(args.warmup + args.steps):
+        rate, cores, sample, _ = oracle_sample(w, inp, per_step)
+        if i >= args.warmup:
+            rates.append(rate)
+    rate = statistics.median(rates)
+    ms = total / (rate * 1e12) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "B": B, "H": H, "S": S, "d": d,
+                                        "P": inp["P"], "causal": inp["causal"]},
+        "tokens_per_s": B * S / (ms / 1e3),
+        "cpu_baseline": {"value": rate, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample + "; each step a bounded sample"},
+        "e2e": {"value": rate, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    w = next(x for x in workloads.ALL if x.name == args.workload)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import long_context_exact_ring_gb300 as ra
+    from long_context_exact_ring_gb300 import build as ra_build
+    ra_build.build()
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    inp = workloads.make(w, device="cuda", keep_fp32=False, seed=w.seed + rank)
+    B, H, S, d, P, causal, sc = (inp[x] for x in ("B", "H", "S", "d", "P", "causal", "scale"))
+    q, k, v = inp["q"], inp["k"], inp["v"]
+    do = inp.get("do")
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
+    if w.backward:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+        ws = torch.empty(ra.bwd_workspace_size(B, H, S, d), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ra.ring_attn_fwd(q, k, v, P, causal, sc, o=o, lse=lse, stream=stream)
+        if w.backward:
+            ra.ring_attn_bwd(q, k, v, o, lse, do, P, causal, sc, dq=dq, dk=dk, dv=dv,
+                             workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if ra.check_status() != ra.RA_OK:
+        raise RuntimeError("a kernel reported a bounded-wait timeout during warm-up")
+
+    # ---- timed region ----------------------------------------------------
+    clocks = ClockSampler(local)
+    ra.profile_enable(True)
+    ra.profile_reset()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    prof = ra.profile_read()
+    ra.profile_enable(False)
+    if ra.check_status() != ra.RA_OK:
+        raise RuntimeError("a kernel reported a bounded-wait timeout in the timed region")
+    ms_total = ev0.elapsed_time(ev1)
+    if dist is not None:
+        t = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    f_fwd, f_bwd = flops(w, B, H, S, d, causal)
+    f_step = f_fwd + f_bwd
+    value = f_step * world / (ms_step / 1e3) / 1e12
+    tokens = B * S * world / (ms_step / 1e3)
+    launches = sum(n for n, _ in prof.values())
+
+    fwd_n, fwd_ms = prof["ring_fwd_kernel"]
+    bwd_n, bwd_ms = prof["ring_bwd_kernel"]
+    fwd_avg = fwd_ms / max(1, fwd_n)
+    bwd_avg = bwd_ms / max(1, bwd_n) if bwd_n else None
+    peaks, peak_src = load_peaks()
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    fwd_tf = f_fwd / (fwd_avg / 1e3) / 1e12
+    passes = {"fwd": {"ms": fwd_avg, "tflops": fwd_tf, "frac_of_peak": fwd_tf / peak_sus}}
+    if bwd_avg:
+        bwd_tf = f_bwd / (bwd_avg / 1e3) / 1e12
+        passes["bwd_main"] = {"ms": bwd_avg, "tflops": bwd_tf, "frac_of_peak": bwd_tf / peak_sus}
+        aux_ms = (prof["bwd_prep_kernel"][1] + prof["dq_convert_kernel"][1]) / max(1, bwd_n)
+        passes["bwd_total"] = {"ms": bwd_avg + aux_ms,
+                               "tflops": f_bwd / ((bwd_avg + aux_ms) / 1e3) / 1e12}
+    # dominant kernel: the one with the largest share of device time
+    dom = max(("ring_fwd_kernel", "ring_bwd_kernel"), key=lambda n: prof[n][1])
+    dom_ms = prof[dom][1] / max(1, prof[dom][0])
+    dom_flop = f_fwd if dom == "ring_fwd_kernel" else f_bwd
+    achieved = dom_flop / (dom_ms / 1e3) / 1e12
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_sus,
+                "unit": "TFLOP/s", "frac": achieved / peak_sus, "traffic": None,
+                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a multi-second step)",
+                "frac_of_burst_peak": achieved / peak_burst}
+
+    # ---- end to end through the public API with host buffers ---------------
+    e2e = None
+    if not args.no_e2e:
+        host_in = {n: t.to("cpu").pin_memory() for n, t in (("q", q), ("k", k), ("v", v))}
+        if w.backward:
+            host_in["do"] = do.to("cpu").pin_memory()
+        outs = [o, lse] + ([dq, dk, dv] if w.backward else [])
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        dev_in = {"q": q, "k": k, "v": v}
+        if w.backward:
+            dev_in["do"] = do
+
+        def e2e_step():
+            for n, h in host_in.items():
+                dev_in[n].copy_(h, non_blocking=True)
+            step()
+            for h, t in zip(host_out, outs):
+                h.copy_(t, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1) / args.e2e_steps
+        if dist is not None:
+            t = torch.tensor([e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": f_step * world / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e_ms,
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in.values()),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out)}
+
+    # ---- CPU oracle baseline (rank 0, one GPU only) ------------------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, cores, sample, _ = oracle_sample(w, inp, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) on device)",
+            "config": {"workload": w.name, "B": B, "H": H, "S": S, "d": d, "P": P,
+                       "causal": causal, "passes": "fwd+bwd" if w.backward else "fwd",
+                       "l2": "inputs larger than L2 (1 GiB per tensor)",
+                       "parallelism": f"replicas x{world}"},
+            "tokens_per_s": tokens,
+            "passes": passes,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "kernels": {n: {"launches": c, "ms": m} for n, (c, m) in prof.items() if c},
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

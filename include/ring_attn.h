@@ -1,0 +1,177 @@
+/*
+ * ring_attn.h -- C ABI of the GB300 (sm_103a) exact ring-attention library
+ * (libringattn.so).
+ *
+ * The method ("Training Long-Context Models Without OOM: Ring Attention",
+ * section "Ring Attention Demystified", steps 1-5; "Context Parallelism"
+ * guide, section 2 "Ring Attention" / "How It Works"): a sequence of S tokens
+ * is split into P equal contiguous chunks of C = S / P tokens.  Query chunk i
+ * meets KV chunk j = (i - t) mod P at ring step t = 0 .. P-1 (step 0 is its
+ * own chunk; every later step receives the left neighbour's K and V).  Each
+ * step's partial attention is folded into running softmax statistics (row
+ * maximum and sum of exponentials), so after P - 1 rotations every query has
+ * attended to the whole sequence and the result is exactly unchunked
+ * attention:
+ *     s_rc  = scale * <q_r, k_c>
+ *     LSE_r = ln sum_{c in A_r} exp(s_rc)          (natural log)
+ *     O_r   = sum_{c in A_r} exp(s_rc - LSE_r) v_c
+ * with A_r = { c <= r } when causal, else all keys.  Causal masking is not
+ * on the pages; the reading used is global-position masking, which skips
+ * chunks j > i and masks key > query inside chunk i.  On one GPU the P ranks
+ * are chunks and the rotation is double-buffered on-chip staging of the next
+ * K/V tile.
+ *
+ * Conventions for every entry point:
+ *   - Tensors are contiguous, row-major [B, H, S, d]; LSE and other per-row
+ *     vectors are [B, H, S].  ra_bf16 holds raw bfloat16 bits.
+ *   - All tensor pointers are DEVICE pointers, 16-byte aligned, owned by the
+ *     caller.  The library allocates no device memory per call; it keeps one
+ *     4-byte status word per device (static device storage).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous on that stream; nothing synchronizes except
+ *     ring_attn_check_status.
+ *   - Arguments are validated before any launch; a bad argument returns
+ *     RA_ERR_INVALID_ARG, a valid but unsupported shape RA_ERR_UNSUPPORTED,
+ *     a failed launch RA_ERR_CUDA (see ring_attn_last_error).  Nothing is
+ *     launched when an error is returned.
+ *   - Shapes with B, H or S equal to 0 are accepted and launch nothing.
+ *   - Every wait inside the kernels is bounded in time; a wait that runs out
+ *     ends the kernel early and sets the device status word, which
+ *     ring_attn_check_status reports as RA_ERR_DEVICE_TIMEOUT.
+ */
+#ifndef RING_ATTN_H
+#define RING_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t ra_bf16;
+
+typedef enum {
+    RA_OK = 0,
+    RA_ERR_INVALID_ARG = -1,
+    RA_ERR_UNSUPPORTED = -2,
+    RA_ERR_CUDA = -3,
+    RA_ERR_DEVICE_TIMEOUT = -4
+} ra_status;
+
+/*
+ * Forward pass of exact ring attention.
+ *   q, k, v  [B, H, S, d] bf16 inputs (read only).
+ *   o        [B, H, S, d] bf16 output: O_r rounded to nearest even.
+ *   lse      [B, H, S] fp32 output: LSE_r (natural log), kept for the
+ *            backward pass.
+ *   P        number of ring chunks, P >= 1 and S % P == 0 (the pages split
+ *            the sequence "equally"; an unequal split is RA_ERR_INVALID_ARG).
+ *   causal   0 or 1.
+ *   scale    finite softmax scale (typically 1/sqrt(d)).
+ *   d        64 or 128 (other values: RA_ERR_UNSUPPORTED).
+ * q, k, v must not alias o or lse.  Chunk lengths need not be multiples of
+ * the 128-row tile: ragged tails are masked.
+ */
+int ring_attn_fwd(const ra_bf16 *q, const ra_bf16 *k, const ra_bf16 *v, ra_bf16 *o, float *lse,
+                  int B, int H, int S, int d, int P, int causal, float scale, void *stream);
+
+/*
+ * Bytes of device workspace ring_attn_bwd needs for this shape: an fp32 dQ
+ * accumulator [B, H, S, d] plus two fp32 row vectors [B, H, S]
+ * (D_r = sum dO_r * O_r and LSE in base 2), each section 256-byte aligned.
+ * Returns 0 for an empty or invalid shape.
+ */
+size_t ring_attn_bwd_workspace_size(int B, int H, int S, int d);
+
+/*
+ * Backward pass.  The pages keep activations for the backward pass and trade
+ * compute for memory by recomputation ("Training Long-Context Models
+ * Without OOM: Ring Attention", sections "Diagnosing the Sequence-Length
+ * OOM" and "Why the Parallelism You Already Have Will Not Work"); the
+ * attention matrix is recomputed from the saved LSE, tile by tile, in the
+ * same ring order.  For the loss L = sum(dO * O):
+ *     P_rc = exp(s_rc - LSE_r) on A_r,  dV = P^T dO,  dP = dO V^T,
+ *     D_r = sum_c dO_rc O_rc,  dS = P * (dP - D),
+ *     dQ = scale dS K,  dK = scale dS^T Q.
+ *   q, k, v, o, dO  [B, H, S, d] bf16 inputs; lse [B, H, S] fp32 from
+ *                   ring_attn_fwd with the same arguments.
+ *   dq, dk, dv      [B, H, S, d] bf16 outputs (overwritten).
+ *   workspace       device buffer of at least
+ *                   ring_attn_bwd_workspace_size(B, H, S, d) bytes, 256-byte
+ *                   aligned, owned by the caller; its contents on entry do
+ *                   not matter and are clobbered.
+ * Other arguments as for ring_attn_fwd.  Inputs must not alias outputs.
+ */
+int ring_attn_bwd(const ra_bf16 *q, const ra_bf16 *k, const ra_bf16 *v, const ra_bf16 *o,
+                  const float *lse, const ra_bf16 *dO, ra_bf16 *dq, ra_bf16 *dk, ra_bf16 *dv,
+                  int B, int H, int S, int d, int P, int causal, float scale, void *workspace,
+                  size_t workspace_bytes, void *stream);
+
+/*
+ * Log-sum-exp merge of two partial attention results of the same query rows
+ * (the merge each ring step performs; "Context Parallelism" guide, section
+ * 2: partial results are merged with the online-softmax statistics):
+ *     m = max(lse_a, lse_b),  w_a = exp(lse_a - m),  w_b = exp(lse_b - m),
+ *     o_out = (w_a o_a + w_b o_b) / (w_a + w_b),  lse_out = m + ln(w_a + w_b).
+ * (o = 0, lse = -inf) is the identity; two -inf rows give (0, -inf).
+ *   o_a, o_b, o_out      [B, H, S, d] fp32 (any d >= 1; 16-byte aligned).
+ *   lse_a, lse_b, lse_out [B, H, S] fp32, natural log (4-byte aligned).
+ * In-place use is allowed: o_out == o_a and lse_out == lse_a.  No other
+ * aliasing.
+ */
+int attn_merge_partials(const float *o_a, const float *lse_a, const float *o_b, const float *lse_b,
+                        float *o_out, float *lse_out, int B, int H, int S, int d, void *stream);
+
+/*
+ * The chunk-level ring schedule the kernels follow, on the host.  For query
+ * chunk i (0 <= i < P) writes, in ring order t = 0, 1, ..., the visited KV
+ * chunks out_j[n] = (i - t) mod P and their kind out_kind[n]: 0 = the query
+ * chunk's own chunk (lower-triangular mask when causal), 1 = a whole chunk.
+ * Causal skips j > i.  Returns the number of visits (P, or i + 1 when
+ * causal), or RA_ERR_INVALID_ARG (bad P or i, or cap too small; null
+ * out_j / out_kind with cap = 0 just returns the count).  Host memory only.
+ */
+int ring_attn_schedule(int P, int causal, int i, int *out_j, int *out_kind, int cap);
+
+/*
+ * Synchronizes `stream`, then reads and clears the current device's status
+ * word.  RA_OK if no kernel reported a problem since the last check,
+ * RA_ERR_DEVICE_TIMEOUT if a bounded wait ran out, RA_ERR_CUDA if the
+ * stream reported an error.
+ */
+int ring_attn_check_status(void *stream);
+
+/* Static, human-readable name of a status code. */
+const char *ring_attn_status_string(int status);
+
+/* Last CUDA error message recorded by this thread (static storage). */
+const char *ring_attn_last_error(void);
+
+/*
+ * Time limit, in nanoseconds, of every bounded wait inside the kernels
+ * launched after this call (default 4e9, i.e. 4 s; 0 restores the default).
+ * A small limit makes a valid run end early with RA_ERR_DEVICE_TIMEOUT
+ * instead of completing; it exists to test that path.  Returns RA_OK.
+ */
+int ring_attn_set_wait_limit_ns(unsigned long long ns);
+
+/*
+ * Kernel timing.  While enabled, every kernel the library launches is
+ * bracketed by a pair of CUDA events on its launch stream.
+ * ring_attn_profile_read synchronizes on the recorded events and returns,
+ * for the kernel named (one of "ring_fwd_kernel", "ring_bwd_kernel",
+ * "bwd_prep_kernel", "dq_convert_kernel", "merge_partials_kernel"), the
+ * number of launches and their summed device time in milliseconds since
+ * the last ring_attn_profile_reset.  Host-side state, process-wide; not for
+ * use inside CUDA graph capture.  RA_ERR_INVALID_ARG for an unknown name.
+ */
+int ring_attn_profile_enable(int on);
+int ring_attn_profile_reset(void);
+int ring_attn_profile_read(const char *kernel, double *total_ms, long long *launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RING_ATTN_H */

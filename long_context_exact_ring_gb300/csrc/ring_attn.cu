@@ -1,0 +1,337 @@
+// ring_attn.cu -- the C-ABI boundary of libringattn.so: argument
+// validation, TMA descriptor set-up, per-device state and kernel launches.
+// Declarations and the contract of every entry point: include/ring_attn.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "ring_attn.h"
+#include "profile.cuh"
+#include "fwd_kernel.cuh"
+#include "bwd_kernel.cuh"
+#include "small_kernels.cuh"
+
+namespace {
+
+// One status word per device (bit flags, see ra::kStatus*).
+__device__ uint32_t g_status_word;
+
+thread_local char g_last_error[256] = "";
+std::atomic<unsigned long long> g_wait_limit_ns{4000000000ull};
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    uint32_t* status = nullptr;   // device address of g_status_word
+    int num_sms = 0;
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int fail_cuda(cudaError_t e, const char* what)
+{
+    std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", what, cudaGetErrorString(e));
+    return RA_ERR_CUDA;
+}
+
+// Per-device set-up, once per device: resolve the status word's device
+// address, raise the kernels' shared-memory limits, find the TMA encoder.
+int device_state(DeviceState** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return RA_ERR_UNSUPPORTED;
+    DeviceState& st = g_dev[dev];
+    if (st.ready) {
+        *out = &st;
+        return RA_OK;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!st.ready) {
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+                return fail_cuda(e == cudaSuccess ? cudaErrorNotSupported : e,
+                                 "cuTensorMapEncodeTiled lookup");
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+        void* addr = nullptr;
+        e = cudaGetSymbolAddress(&addr, g_status_word);
+        if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(status)");
+        st.status = static_cast<uint32_t*>(addr);
+        e = cudaMemset(st.status, 0, sizeof(uint32_t));
+        if (e != cudaSuccess) return fail_cuda(e, "cudaMemset(status)");
+        e = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
+        e = cudaFuncSetAttribute(ra::fwd::ring_fwd_kernel<64>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 ra::fwd::Cfg<64>::kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(ra::fwd::ring_fwd_kernel<128>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     ra::fwd::Cfg<128>::kSmemBytes);
+        if (e == cudaSuccess) e = ra::bwd::configure_kernels();
+        if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute");
+        st.ready = true;
+    }
+    *out = &st;
+    return RA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 3-D tiled map over a [B*H, S, d] bf16 tensor: box of 64 columns x `rows`
+// rows x 1 head, 128-byte swizzle.  Rows past S read as zero.
+int make_map(CUtensorMap* map, const void* ptr, int BH, int S, int d, int rows)
+{
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)S, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)S * d * 2};
+    cuuint32_t box[3] = {64u, (cuuint32_t)rows, 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        std::snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed (%d)",
+                      (int)r);
+        return RA_ERR_CUDA;
+    }
+    return RA_OK;
+}
+
+// Shape checks shared by the forward and backward passes.
+int check_shape(int B, int H, int S, int d, int P, int causal, float scale)
+{
+    if (B < 0 || H < 0 || S < 0 || P < 1) return RA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return RA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return RA_ERR_INVALID_ARG;
+    if (S % P != 0) return RA_ERR_INVALID_ARG;   // equal contiguous chunks only
+    if (d != 64 && d != 128) return RA_ERR_UNSUPPORTED;
+    if ((long long)B * H > (1ll << 30)) return RA_ERR_UNSUPPORTED;
+    return RA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ring_attn_status_string(int status)
+{
+    switch (status) {
+    case RA_OK: return "RA_OK";
+    case RA_ERR_INVALID_ARG: return "RA_ERR_INVALID_ARG";
+    case RA_ERR_UNSUPPORTED: return "RA_ERR_UNSUPPORTED";
+    case RA_ERR_CUDA: return "RA_ERR_CUDA";
+    case RA_ERR_DEVICE_TIMEOUT: return "RA_ERR_DEVICE_TIMEOUT";
+    default: return "RA_UNKNOWN_STATUS";
+    }
+}
+
+const char* ring_attn_last_error(void) { return g_last_error; }
+
+int ring_attn_set_wait_limit_ns(unsigned long long ns)
+{
+    g_wait_limit_ns.store(ns == 0 ? 4000000000ull : ns);
+    return RA_OK;
+}
+
+int ring_attn_schedule(int P, int causal, int i, int* out_j, int* out_kind, int cap)
+{
+    if (P < 1 || i < 0 || i >= P || (causal != 0 && causal != 1) || cap < 0)
+        return RA_ERR_INVALID_ARG;
+    const int count = causal ? i + 1 : P;
+    if (cap == 0 && !out_j && !out_kind) return count;
+    if (!out_j || !out_kind || cap < count) return RA_ERR_INVALID_ARG;
+    int n = 0;
+    for (int t = 0; t < P; ++t) {
+        const int j = ((i - t) % P + P) % P;
+        if (causal && j > i) continue;
+        out_j[n] = j;
+        out_kind[n] = (j == i) ? 0 : 1;
+        ++n;
+    }
+    return n;
+}
+
+int ring_attn_fwd(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, ra_bf16* o, float* lse,
+                  int B, int H, int S, int d, int P, int causal, float scale, void* stream)
+{
+    int rc = check_shape(B, H, S, d, P, causal, scale);
+    if (rc != RA_OK) return rc;
+    if ((long long)B * H * S == 0) return RA_OK;
+    if (!q || !k || !v || !o || !lse) return RA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return RA_ERR_INVALID_ARG;
+    const int C = S / P;
+    const long long pairs = (C + ra::fwd::kRowsPerCta - 1) / ra::fwd::kRowsPerCta;
+    const long long grid = (long long)B * H * P * pairs;
+    if (grid > 0x7fffffffll) return RA_ERR_UNSUPPORTED;
+
+    DeviceState* st = nullptr;
+    rc = device_state(&st);
+    if (rc != RA_OK) return rc;
+    CUtensorMap mq, mk, mv;
+    const int BH = B * H;
+    if ((rc = make_map(&mq, q, BH, S, d, ra::fwd::kBM)) != RA_OK) return rc;
+    if ((rc = make_map(&mk, k, BH, S, d, ra::fwd::kBN)) != RA_OK) return rc;
+    if ((rc = make_map(&mv, v, BH, S, d, ra::fwd::kBN)) != RA_OK) return rc;
+
+    ra::fwd::FwdParams prm;
+    prm.o = reinterpret_cast<__nv_bfloat16*>(o);
+    prm.lse = lse;
+    prm.S = S;
+    prm.P = P;
+    prm.C = C;
+    prm.causal = causal;
+    prm.pairs_per_chunk = (int)pairs;
+    prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    prm.status = st->status;
+    prm.wait_limit_ns = g_wait_limit_ns.load();
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    ra::prof::Scope ps(ra::prof::kFwd, s);
+    if (d == 128)
+        ra::fwd::ring_fwd_kernel<128><<<(unsigned)grid, ra::fwd::kThreads,
+                                        ra::fwd::Cfg<128>::kSmemBytes, s>>>(mq, mk, mv, prm);
+    else
+        ra::fwd::ring_fwd_kernel<64><<<(unsigned)grid, ra::fwd::kThreads,
+                                       ra::fwd::Cfg<64>::kSmemBytes, s>>>(mq, mk, mv, prm);
+    ps.done();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail_cuda(e, "ring_fwd_kernel launch");
+    return RA_OK;
+}
+
+size_t ring_attn_bwd_workspace_size(int B, int H, int S, int d)
+{
+    if (B <= 0 || H <= 0 || S <= 0 || d <= 0) return 0;
+    return ra::bwd::workspace_bytes(B, H, S, d);
+}
+
+int ring_attn_bwd(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, const ra_bf16* o,
+                  const float* lse, const ra_bf16* dO, ra_bf16* dq, ra_bf16* dk, ra_bf16* dv,
+                  int B, int H, int S, int d, int P, int causal, float scale, void* workspace,
+                  size_t workspace_bytes, void* stream)
+{
+    int rc = check_shape(B, H, S, d, P, causal, scale);
+    if (rc != RA_OK) return rc;
+    if ((long long)B * H * S == 0) return RA_OK;
+    if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)
+        return RA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return RA_ERR_INVALID_ARG;
+    if (workspace_bytes < ra::bwd::workspace_bytes(B, H, S, d)) return RA_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    rc = device_state(&st);
+    if (rc != RA_OK) return rc;
+    ra::bwd::Launch L;
+    L.q = q; L.k = k; L.v = v; L.o = o; L.lse = lse; L.dO = dO;
+    L.dq = dq; L.dk = dk; L.dv = dv;
+    L.B = B; L.H = H; L.S = S; L.d = d; L.P = P; L.causal = causal; L.scale = scale;
+    L.workspace = workspace;
+    L.status = st->status;
+    L.num_sms = st->num_sms;
+    L.wait_limit_ns = g_wait_limit_ns.load();
+    L.stream = static_cast<cudaStream_t>(stream);
+    L.encode = [](CUtensorMap* m, const void* p, int BH, int S_, int d_, int rows) {
+        return make_map(m, p, BH, S_, d_, rows);
+    };
+    cudaError_t e = cudaSuccess;
+    rc = ra::bwd::launch(L, &e);
+    if (rc == RA_ERR_CUDA) return fail_cuda(e, "ring_bwd launch");
+    return rc;
+}
+
+int attn_merge_partials(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b,
+                        float* o_out, float* lse_out, int B, int H, int S, int d, void* stream)
+{
+    if (B < 0 || H < 0 || S < 0 || d < 1) return RA_ERR_INVALID_ARG;
+    const long long rows = (long long)B * H * S;
+    if (rows == 0) return RA_OK;
+    if (!o_a || !lse_a || !o_b || !lse_b || !o_out || !lse_out) return RA_ERR_INVALID_ARG;
+    if (!aligned16(o_a) || !aligned16(o_b) || !aligned16(o_out) ||
+        (reinterpret_cast<uintptr_t>(lse_a) & 3u) || (reinterpret_cast<uintptr_t>(lse_b) & 3u) ||
+        (reinterpret_cast<uintptr_t>(lse_out) & 3u))
+        return RA_ERR_INVALID_ARG;
+    // Only the documented in-place form may alias.
+    if (o_out == o_b || lse_out == lse_b || (const void*)o_out == (const void*)lse_a)
+        return RA_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != RA_OK) return rc;
+    const long long warps_needed = rows;
+    long long blocks = (warps_needed + 7) / 8;
+    const long long cap = (long long)st->num_sms * 16;
+    if (blocks > cap) blocks = cap;
+    ra::prof::Scope ps(ra::prof::kMerge, static_cast<cudaStream_t>(stream));
+    ra::merge_partials_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        o_a, lse_a, o_b, lse_b, o_out, lse_out, rows, d);
+    ps.done();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail_cuda(e, "merge_partials_kernel launch");
+    return RA_OK;
+}
+
+int ring_attn_profile_enable(int on)
+{
+    ra::prof::g_on.store(on ? 1 : 0);
+    return RA_OK;
+}
+
+int ring_attn_profile_reset(void)
+{
+    ra::prof::reset();
+    return RA_OK;
+}
+
+int ring_attn_profile_read(const char* kernel, double* total_ms, long long* launches)
+{
+    if (!kernel || !total_ms || !launches) return RA_ERR_INVALID_ARG;
+    ra::prof::collect();
+    for (int k = 0; k < ra::prof::kKinds; ++k) {
+        if (std::strcmp(kernel, ra::prof::kind_name(k)) == 0) {
+            std::lock_guard<std::mutex> lock(ra::prof::g_mu);
+            *total_ms = ra::prof::g_ms[k];
+            *launches = ra::prof::g_count[k];
+            return RA_OK;
+        }
+    }
+    return RA_ERR_INVALID_ARG;
+}
+
+int ring_attn_check_status(void* stream)
+{
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != RA_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
+    uint32_t word = 0;
+    e = cudaMemcpyAsync(&word, st->status, sizeof(word), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(st->status, 0, sizeof(uint32_t), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail_cuda(e, "status read");
+    return word ? RA_ERR_DEVICE_TIMEOUT : RA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,125 @@
+// small_kernels.cuh -- the memory-bound kernels of the library:
+//   merge_partials_kernel  log-sum-exp merge of two partial attentions
+//   bwd_prep_kernel        D_r = sum_k dO_rk O_rk and LSE in log2 units
+//   dq_convert_kernel      fp32 dQ accumulator -> bf16 dQ
+#pragma once
+
+#include "sm103_ptx.cuh"
+
+namespace ra {
+
+// Merge of two partial results of the same query rows ("Context
+// Parallelism" guide, section 2: partial attention results merged with the
+// online-softmax statistics; "Training Long-Context Models Without OOM:
+// Ring Attention", "Ring Attention Demystified": running row maximum and
+// sum of exponentials):
+//     m = max(lse_a, lse_b),  w_a = exp(lse_a - m),  w_b = exp(lse_b - m)
+//     O = (w_a O_a + w_b O_b) / (w_a + w_b),  lse = m + ln(w_a + w_b).
+// (0, -inf) is the identity; two -inf rows give (0, -inf).
+//
+// One warp per row, grid-stride over rows.  The row's LSE pair is read by
+// every lane before lane 0 writes the merged LSE, so lse_out may alias
+// lse_a (and o_out may alias o_a: each element is read, then written, by
+// the same lane).
+__global__ void __launch_bounds__(256)
+merge_partials_kernel(const float* o_a, const float* lse_a, const float* __restrict__ o_b,
+                      const float* lse_b, float* o_out, float* lse_out, long long rows, int d)
+{
+    const long long warp_global = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long warp_count = ((long long)gridDim.x * blockDim.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const bool vec4 = (d & 3) == 0;
+    for (long long r = warp_global; r < rows; r += warp_count) {
+        const float la = lse_a[r];
+        const float lb = lse_b[r];
+        const float m = fmaxf(la, lb);
+        float wa, wb, inv;
+        if (m == -INFINITY) {
+            wa = 0.f; wb = 0.f; inv = 0.f;
+        } else {
+            wa = expf(la - m);
+            wb = expf(lb - m);
+            inv = 1.f / (wa + wb);
+        }
+        const float ca = wa * inv, cb = wb * inv;
+        const size_t base = (size_t)r * d;
+        if (vec4) {
+            const float4* a4 = reinterpret_cast<const float4*>(o_a + base);
+            const float4* b4 = reinterpret_cast<const float4*>(o_b + base);
+            float4* o4 = reinterpret_cast<float4*>(o_out + base);
+            for (int x = lane; x < (d >> 2); x += 32) {
+                const float4 a = a4[x], b = b4[x];
+                o4[x] = make_float4(ca * a.x + cb * b.x, ca * a.y + cb * b.y, ca * a.z + cb * b.z,
+                                    ca * a.w + cb * b.w);
+            }
+        } else {
+            for (int x = lane; x < d; x += 32) o_out[base + x] = ca * o_a[base + x] + cb * o_b[base + x];
+        }
+        __syncwarp();
+        if (lane == 0) lse_out[r] = (m == -INFINITY) ? -INFINITY : m + logf(wa + wb);
+    }
+}
+
+// Backward preparation, one warp per row:
+//   D_r = sum_k dO_rk * O_rk (fp32 accumulate of the bf16 inputs) and
+//   lse2_r = LSE_r * log2(e) (the exponent base the main kernel uses).
+template <int D>
+__global__ void __launch_bounds__(256)
+bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
+                const float* __restrict__ lse, float* __restrict__ Dvec, float* __restrict__ lse2,
+                long long rows)
+{
+    const long long warp_global = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long warp_count = ((long long)gridDim.x * blockDim.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    constexpr int kPer = D / 32;   // elements per lane (2 or 4)
+    for (long long r = warp_global; r < rows; r += warp_count) {
+        const size_t base = (size_t)r * D + (size_t)lane * kPer;
+        float acc = 0.f;
+        if constexpr (kPer == 4) {
+            const uint2 a = *reinterpret_cast<const uint2*>(o + base);
+            const uint2 b = *reinterpret_cast<const uint2*>(dO + base);
+            const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                const float2 fa = __bfloat1622float2(a2[x]);
+                const float2 fb = __bfloat1622float2(b2[x]);
+                acc = fmaf(fa.x, fb.x, acc);
+                acc = fmaf(fa.y, fb.y, acc);
+            }
+        } else {
+            const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + base);
+            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(dO + base);
+            const float2 fa = __bfloat1622float2(a);
+            const float2 fb = __bfloat1622float2(b);
+            acc = fmaf(fa.x, fb.x, acc);
+            acc = fmaf(fa.y, fb.y, acc);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) {
+            Dvec[r] = acc;
+            lse2[r] = lse[r] * 1.4426950408889634f;
+        }
+    }
+}
+
+// dQ (fp32 accumulator, already scaled) -> bf16, 8 elements per thread.
+__global__ void __launch_bounds__(256)
+dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, long long n8)
+{
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
+        const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+        const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+        uint4 out;
+        out.x = pack_bf16x2(a.x, a.y);
+        out.y = pack_bf16x2(a.z, a.w);
+        out.z = pack_bf16x2(b.x, b.y);
+        out.w = pack_bf16x2(b.z, b.w);
+        reinterpret_cast<uint4*>(dq)[i] = out;
+    }
+}
+
+}  // namespace ra

@@ -67,12 +67,15 @@ ALL = [TINY_F32, FWD_CAUSAL_32K, FWD_CAUSAL_128K, FWD_PEAKED_64K, FWDBWD_CAUSAL_
 
 
 def make(w: Workload, *, B=None, H=None, S=None, d=None, P=None, causal=None,
-         seed=None, backward=None):
+         seed=None, backward=None, device="cpu", keep_fp32=True):
     """Draw the inputs of workload ``w`` (optionally with overridden sizes).
 
     Returns a dict with fp32 tensors ``q32, k32, v32`` (and ``do32``) exactly
-    as drawn, and their bf16 roundings ``q, k, v`` (and ``do``), all on CPU,
-    contiguous [B, H, S, d], plus the resolved shape fields.
+    as drawn, and their bf16 roundings ``q, k, v`` (and ``do``), contiguous
+    [B, H, S, d], plus the resolved shape fields.  With ``device="cuda"`` the
+    same recipe runs with a generator on that device (a different random
+    stream from the CPU one; used where only throughput is measured) and
+    ``keep_fp32=False`` drops the fp32 copies.
     """
     B = w.B if B is None else B
     H = w.H if H is None else H
@@ -82,24 +85,26 @@ def make(w: Workload, *, B=None, H=None, S=None, d=None, P=None, causal=None,
     causal = w.causal if causal is None else causal
     seed = w.seed if seed is None else seed
     backward = w.backward if backward is None else backward
-    g = torch.Generator("cpu").manual_seed(seed)
+    g = torch.Generator(device).manual_seed(seed)
     shape = (B, H, S, d)
-    q32 = torch.randn(shape, generator=g, dtype=torch.float32)
-    k32 = torch.randn(shape, generator=g, dtype=torch.float32)
-    if w.v_uniform:
-        v32 = torch.rand(shape, generator=g, dtype=torch.float32) * 2 - 1
-    else:
-        v32 = torch.randn(shape, generator=g, dtype=torch.float32)
-    if w.peaked_keys:
-        k32[:, :, 0::64, :] *= 8.0
-    out = dict(B=B, H=H, S=S, d=d, P=P, causal=causal, scale=1.0 / math.sqrt(d),
-               q32=q32, k32=k32, v32=v32,
-               q=q32.to(torch.bfloat16), k=k32.to(torch.bfloat16),
-               v=v32.to(torch.bfloat16))
+    out = dict(B=B, H=H, S=S, d=d, P=P, causal=causal, scale=1.0 / math.sqrt(d))
+
+    def draw(name, uniform=False, peaked=False):
+        if uniform:
+            x = torch.rand(shape, generator=g, dtype=torch.float32, device=device) * 2 - 1
+        else:
+            x = torch.randn(shape, generator=g, dtype=torch.float32, device=device)
+        if peaked:
+            x[:, :, 0::64, :] *= 8.0
+        out[name] = x.to(torch.bfloat16)
+        if keep_fp32:
+            out[name + "32"] = x
+
+    draw("q")
+    draw("k", peaked=w.peaked_keys)
+    draw("v", uniform=w.v_uniform)
     if backward:
-        do32 = torch.randn(shape, generator=g, dtype=torch.float32)
-        out["do32"] = do32
-        out["do"] = do32.to(torch.bfloat16)
+        draw("do")
     return out
 
 
