@@ -60,6 +60,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle sample")
+    ap.add_argument("--seq", type=int, default=None,
+                    help="override S (smaller cases for profiling; not a bench line)")
+    ap.add_argument("--heads", type=int, default=None, help="override H (profiling)")
     return ap.parse_args()
 
 
@@ -241,7 +244,8 @@ def main():
         if dist is not None:
             dist.barrier()
 
-    inp = workloads.make(w, device="cuda", keep_fp32=False, seed=w.seed + rank)
+    inp = workloads.make(w, device="cuda", keep_fp32=False, seed=w.seed + rank,
+                         S=args.seq, H=args.heads)
     B, H, S, d, P, causal, sc = (inp[x] for x in ("B", "H", "S", "d", "P", "causal", "scale"))
     q, k, v = inp["q"], inp["k"], inp["v"]
     do = inp.get("do")

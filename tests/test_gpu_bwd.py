@@ -11,7 +11,7 @@ import torch
 
 import oracle
 import workloads
-from _parity import assert_grad_close, f64
+from _parity import assert_grad_close, assert_grad_close_scaled, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -63,9 +63,9 @@ def test_bwd_peaked_keys(ra):
     inp = workloads.make(w, B=1, H=2, S=2048, P=8, backward=True)
     q, k, v, do, o, lse, dq, dk, dv = _fwd_bwd(ra, inp)
     dq_r, dk_r, dv_r, _, _ = oracle.bwd(f64(q), f64(k), f64(v), f64(do), False, inp["scale"])
-    assert_grad_close(f64(dq), dq_r, "dQ")
-    assert_grad_close(f64(dk), dk_r, "dK")
-    assert_grad_close(f64(dv), dv_r, "dV")
+    assert_grad_close_scaled(f64(dq), dq_r, "dQ")
+    assert_grad_close_scaled(f64(dk), dk_r, "dK")
+    assert_grad_close_scaled(f64(dv), dv_r, "dV")
 
 
 def test_bwd_repeatable_workspace_reuse(ra):
