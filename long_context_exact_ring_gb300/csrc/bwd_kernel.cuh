@@ -16,26 +16,31 @@
 // chunk j is visited by query chunk i at ring step t = (i - j) mod P.  Causal
 // drops i < j and, inside chunk j, query tiles wholly above the diagonal.
 //
-// Per query tile, on the tensor core (all bf16 x bf16 -> fp32):
-//   S^T  = K Q^T      [keys x queries]   -> TMEM S   (A = K, B = Q, K-major)
-//   dP^T = V dO^T     [keys x queries]   -> TMEM dP  (A = V, B = dO, K-major)
-//   dV  += P^T dO     [keys x d]          A = P^T (bf16, TMEM), B = dO (MN-major)
-//   dK  += dS^T Q     [keys x d]          A = dS^T (bf16, TMEM), B = Q (MN-major)
-//   dQ_t = dS K       [queries x d]       A = dS (smem, MN-major), B = K (MN-major)
+// Per query tile, on the tensor core (bf16 x bf16 -> fp32), in issue order:
+//   S^T  = K Q^T      [keys x queries]  -> TMEM S    (A = K, B = Q, K-major)
+//   dP^T = V dO^T     [keys x queries]  -> TMEM dP   (A = V, B = dO, K-major)
+//   dV  += P^T dO     [keys x d]         A = P^T (bf16 in TMEM), B = dO (MN-major)
+//   dQ_t = dS K       [queries x d]     -> TMEM S    A = dS (smem, MN-major), B = K (MN-major)
+//   dK  += dS^T Q     [keys x d]         A = dS^T (bf16 in TMEM), B = Q (MN-major)
 // TMEM (512 columns): S [0,128), dP [128,256), dV [256,256+D), dK after it.
-// P^T (bf16) overwrites S[0,64) and dS^T overwrites dP[0,64); the dQ tile
-// lands in the free upper halves S[64,128) (d columns 0..63) and dP[64,128)
-// (d columns 64..127), from where four drain warps move it into the fp32 dQ
-// accumulator in global memory with vector reductions.
+// Softmax warpgroup h (query columns 64h..64h+63) writes its bf16 P^T over
+// S columns [64h, 64h+32) and its dS^T over dP columns [64h, 64h+32) --
+// only columns it has read itself, so the two warpgroups never wait on each
+// other.  The dQ tile reuses the whole S region once dV has consumed P^T
+// (tcgen05 MMAs of a CTA run in issue order); four drain warps copy it out
+// of TMEM while dK runs and reduce it into the fp32 dQ accumulator in global
+// memory, and the next S^T waits only for that copy.
 //
-// CTA layout (448 threads):
-//   warp 0       TMA producer (K, V once; Q and dO tiles in ring order).
-//   warp 1       TMEM allocator and MMA issuer.
-//   warps 2-9    softmax-gradient: thread = key row; warps 2-5 take query
-//                columns 0..63, warps 6-9 columns 64..127; epilogue dV
-//                (warps 2-5) and dK (warps 6-9).
-//   warps 10-13  dQ drain: thread = query row.
+// CTA layout (512 threads, four warpgroups):
+//   WG0  warp 0 TMA producer (K, V once; Q, dO, LSE2, D tiles in ring order),
+//        warp 1 TMEM allocator and MMA issuer, warps 2-3 idle.
+//   WG1  P^T / dS^T for query columns 0..63 (thread = key row); epilogue dV.
+//   WG2  the same for columns 64..127; epilogue dK.
+//   WG3  dQ drain (thread = query row).
+// Registers: 128 per thread (512 threads, one CTA per SM).
 #pragma once
+
+#include <cstring>
 
 #include "sm103_ptx.cuh"
 #include "small_kernels.cuh"
@@ -46,7 +51,7 @@ namespace bwd {
 
 constexpr int kBK = 128;        // keys per CTA
 constexpr int kBQ = 128;        // queries per streamed tile
-constexpr int kThreads = 448;
+constexpr int kThreads = 512;
 
 template <int D>
 struct Cfg {
@@ -54,14 +59,15 @@ struct Cfg {
     static constexpr int kBoxes = D / 64;
     static constexpr int kBoxBytes = 64 * 128 * 2;          // 16 KB: 128 rows x 64 bf16
     static constexpr int kTileBytes = 128 * D * 2;
-    static constexpr int kStages = 2;                       // Q / dO stages
+    static constexpr int kStages = 2;                       // Q / dO / row stages
+    static constexpr int kRowBytes = kBQ * 4;               // one LSE2 or D row tile
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kOffK + kTileBytes;
     static constexpr int kOffQ = kOffV + kTileBytes;
     static constexpr int kOffDO = kOffQ + kStages * kTileBytes;
     static constexpr int kOffDS = kOffDO + kStages * kTileBytes;        // 128 x 128 bf16
-    static constexpr int kOffRow = kOffDS + 2 * kBoxBytes;              // lse2 / D staging
-    static constexpr int kOffBar = kOffRow + 2 * 2 * kBQ * 4;
+    static constexpr int kOffRow = kOffDS + 2 * kBoxBytes;              // [stage][lse2 | D]
+    static constexpr int kOffBar = kOffRow + kStages * 2 * kRowBytes;
     static constexpr int kBarBytes = 256;
     static constexpr int kSmemBytes = kOffBar + kBarBytes;
     static constexpr uint32_t kTmemCols = 512;
@@ -72,8 +78,8 @@ struct Cfg {
 };
 
 struct BwdParams {
-    const float* lse2;      // [B*H*S] LSE * log2(e)
-    const float* Dvec;      // [B*H*S]
+    const float* lse2;      // [B*H, S] LSE * log2(e)   (read directly when rows are not TMA-able)
+    const float* Dvec;      // [B*H, S]
     float* dq_acc;          // [B*H*S, D] fp32, pre-zeroed
     __nv_bfloat16* dk;      // [B*H*S, D]
     __nv_bfloat16* dv;
@@ -88,13 +94,12 @@ struct BwdParams {
 // i >= j and, in chunk j, tiles from kt on.
 struct QTiles {
     int P, C, j, causal, T, kt;
-    int i, qt, qt_first;
+    int i, qt;
     __device__ __forceinline__ void init(int P_, int C_, int j_, int causal_, int T_, int kt_)
     {
         P = P_; C = C_; j = j_; causal = causal_; T = T_; kt = kt_;
         i = j;
-        qt_first = causal ? kt : 0;
-        qt = qt_first;
+        qt = causal ? kt : 0;
     }
     __device__ __forceinline__ int total() const
     {
@@ -110,10 +115,14 @@ struct QTiles {
     }
 };
 
-template <int D>
+// kRowTma: the per-query LSE2 / D rows arrive by TMA with the Q / dO tile
+// (needs C % 4 == 0 for 16-byte aligned boxes); otherwise the softmax
+// threads read them from global memory.
+template <int D, bool kRowTma>
 __global__ void __launch_bounds__(kThreads, 1)
 ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+                const __grid_constant__ CUtensorMap map_lse2, const __grid_constant__ CUtensorMap map_dvec,
                 const BwdParams p)
 {
     using CF = Cfg<D>;
@@ -128,8 +137,7 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     const uint32_t sQ = base + CF::kOffQ;
     const uint32_t sDO = base + CF::kOffDO;
     const uint32_t sDS = base + CF::kOffDS;
-    float* row_lse2 = reinterpret_cast<float*>(smem + CF::kOffRow);        // [2][128]
-    float* row_D = reinterpret_cast<float*>(smem + CF::kOffRow + 2 * kBQ * 4);
+    const uint32_t sRow = base + CF::kOffRow;
     const uint32_t bar0 = base + CF::kOffBar;
     const uint32_t bar_kv = bar0;
     auto bar_qdo_full = [&](int s) { return bar0 + 8u * (1 + s); };
@@ -142,12 +150,12 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     const uint32_t bar_dq_free = bar0 + 8u * 10;
     const uint32_t bar_kv_final = bar0 + 8u * 11;
     const uint32_t bar_drain = bar0 + 8u * 12;
-    const uint32_t bar_group = bar0 + 8u * 13;   // rendezvous of the 256 softmax threads
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + CF::kOffBar + 192);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + CF::kOffBar + 200);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int wg = warp >> 2;
 
     // ---- work item: (b*H + h, KV chunk j, key tile kt), heaviest first ----
     const int T = p.tiles_per_chunk;
@@ -176,7 +184,6 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         mbar_init(bar_dq_free, 128);
         mbar_init(bar_kv_final, 1);
         mbar_init(bar_drain, 1);
-        mbar_init(bar_group, 256);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -192,13 +199,17 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     qi.init(p.P, p.C, chunk_j, p.causal, T, kt);
     const int NT = qi.total();
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA
-        if (lane == 0) {
+    if (wg == 0) {
+        if (warp == 0 && lane == 0) {
+            // -------------------------------------------------------- TMA
             tma_prefetch_desc(&map_q);
             tma_prefetch_desc(&map_k);
             tma_prefetch_desc(&map_v);
             tma_prefetch_desc(&map_do);
+            if constexpr (kRowTma) {
+                tma_prefetch_desc(&map_lse2);
+                tma_prefetch_desc(&map_dvec);
+            }
             mbar_arrive_expect_tx(bar_kv, 2 * CF::kTileBytes);
             for (int x = 0; x < CF::kBoxes; ++x) {
                 tma_load_3d(sK + x * CF::kBoxBytes, &map_k, bar_kv, 64 * x, k0, bh);
@@ -207,18 +218,24 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             int issued[CF::kStages];
             for (int s = 0; s < CF::kStages; ++s) issued[s] = -1;
             bool ok = true;
+            constexpr uint32_t kStageTx = 2 * CF::kTileBytes + (kRowTma ? 2 * CF::kRowBytes : 0);
             for (int n = 0; n < NT; ++n, qi.next()) {
                 const int s = n % CF::kStages;
                 const uint32_t ph = (uint32_t)(n / CF::kStages) & 1u;
                 ok = mbar_wait(bar_qdo_empty(s), ph ^ 1u, wc);
                 if (!ok) break;
                 const int q0 = qi.q_start();
-                mbar_arrive_expect_tx(bar_qdo_full(s), 2 * CF::kTileBytes);
+                mbar_arrive_expect_tx(bar_qdo_full(s), kStageTx);
                 for (int x = 0; x < CF::kBoxes; ++x) {
                     tma_load_3d(sQ + s * CF::kTileBytes + x * CF::kBoxBytes, &map_q,
                                 bar_qdo_full(s), 64 * x, q0, bh);
                     tma_load_3d(sDO + s * CF::kTileBytes + x * CF::kBoxBytes, &map_do,
                                 bar_qdo_full(s), 64 * x, q0, bh);
+                }
+                if constexpr (kRowTma) {
+                    tma_load_2d(sRow + s * 2 * CF::kRowBytes, &map_lse2, bar_qdo_full(s), q0, bh);
+                    tma_load_2d(sRow + s * 2 * CF::kRowBytes + CF::kRowBytes, &map_dvec,
+                                bar_qdo_full(s), q0, bh);
                 }
                 issued[s] = (int)ph;
             }
@@ -230,13 +247,11 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 for (int s = 0; s < CF::kStages; ++s)
                     if (issued[s] >= 0) mbar_wait(bar_qdo_full(s), (uint32_t)issued[s], drain);
             }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA
-        if (lane == 0) {
+        } else if (warp == 1 && lane == 0) {
+            // -------------------------------------------------------- MMA
             constexpr uint32_t idesc_kq = idesc_bf16_f32(kBK, kBQ, false, false);   // S^T, dP^T
             constexpr uint32_t idesc_kd = idesc_bf16_f32(kBK, D, false, true);      // dV, dK
-            constexpr uint32_t idesc_qd = idesc_bf16_f32(kBQ, 64, true, true);      // dQ halves
+            constexpr uint32_t idesc_qd = idesc_bf16_f32(kBQ, D, true, true);       // dQ tile
             // C = A(smem, K-major) * B(smem, K-major)^T over the head dim.
             auto mma_kmajor = [&](uint32_t d_tmem, uint32_t sa, uint32_t sb) {
 #pragma unroll
@@ -246,11 +261,12 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                                 sdesc_sw128(sb + off, 16, 1024), idesc_kq, kk > 0 ? 1u : 0u);
                 }
             };
-            // C += A(TMEM bf16, keys x queries) * B(smem, queries x D, MN-major)
+            // C += A(TMEM bf16: query columns 0..63 at a_tmem, 64..127 at
+            // a_tmem + 64) * B(smem, queries x D, MN-major).
             auto mma_ts = [&](uint32_t d_tmem, uint32_t a_tmem, uint32_t sb, bool first) {
 #pragma unroll
                 for (int kk = 0; kk < kBQ / 16; ++kk)
-                    mma_bf16_ts(d_tmem, a_tmem + 8u * kk,
+                    mma_bf16_ts(d_tmem, a_tmem + (kk >> 2) * 64u + 8u * (kk & 3),
                                 sdesc_sw128(sb + kk * 2048, CF::kBoxBytes, 1024), idesc_kd,
                                 (first && kk == 0) ? 0u : 1u);
             };
@@ -276,19 +292,16 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 ok = mbar_wait(bar_ds_ready, par, wc);
                 if (!ok) break;
                 tc_fence_after();
-                mma_ts(tmem + CF::kColDK, tmem + CF::kColDP, qs, n == 0);
-                // dQ tile = dS K: A is dS^T stored [key][query] (queries
-                // contiguous, MN-major), B is the K tile (d contiguous).
+                // dQ tile = dS K into the S region (P^T there was consumed by
+                // dV, issued before).  A is dS^T stored [key][query] (queries
+                // contiguous, MN-major); B is the K tile (d contiguous).
 #pragma unroll
-                for (int h = 0; h < CF::kBoxes; ++h) {
-                    const uint32_t d_tmem = tmem + (h == 0 ? CF::kColS : CF::kColDP) + 64u;
-#pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        mma_bf16_ss(d_tmem, sdesc_sw128(sDS + kk * 2048, CF::kBoxBytes, 1024),
-                                    sdesc_sw128(sK + h * CF::kBoxBytes + kk * 2048, CF::kBoxBytes, 1024),
-                                    idesc_qd, kk > 0 ? 1u : 0u);
-                }
+                for (int kk = 0; kk < kBK / 16; ++kk)
+                    mma_bf16_ss(tmem + CF::kColS, sdesc_sw128(sDS + kk * 2048, CF::kBoxBytes, 1024),
+                                sdesc_sw128(sK + kk * 2048, CF::kBoxBytes, 1024), idesc_qd,
+                                kk > 0 ? 1u : 0u);
                 mma_commit(bar_dq_full);
+                mma_ts(tmem + CF::kColDK, tmem + CF::kColDP, qs, n == 0);
                 mma_commit(bar_qdo_empty(s));
             }
             if (ok) mma_commit(bar_kv_final);
@@ -298,73 +311,78 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             drain.abort_flag = &dummy;
             mbar_wait(bar_drain, 0, drain);
         }
-    } else if (warp < 10) {
+    } else if (wg <= 2) {
         // ------------------------------------ P^T, dS^T; epilogue dV / dK
-        const int half = (warp - 2) >> 2;                // query columns [64 half, +64)
+        const int half = wg - 1;                         // query columns [64 half, +64)
         const uint32_t quarter = (uint32_t)(warp & 3);
         const int kr = (int)quarter * 32 + lane;         // key row in the tile
         const int kpos = k0 + kr;
         const bool key_ok = kpos < k_end;
-        const int tid = threadIdx.x - 64;                // 0..255
         const uint32_t tS = tmem_addr(tmem, quarter * 32, CF::kColS + 64u * half);
         const uint32_t tDP = tmem_addr(tmem, quarter * 32, CF::kColDP + 64u * half);
-        const uint32_t tPo = tmem_addr(tmem, quarter * 32, CF::kColS + 32u * half);
-        const uint32_t tDSo = tmem_addr(tmem, quarter * 32, CF::kColDP + 32u * half);
         const float sl2 = p.scale_log2;
         bool ok = true;
-        // Bounded rendezvous of the 256 softmax threads (an mbarrier used as a
-        // barrier): a thread that gives up cannot leave the others waiting
-        // forever.
-        uint32_t group_phase = 0;
-        auto group_sync = [&]() -> bool {
-            mbar_arrive(bar_group);
-            const bool r = __all_sync(0xffffffffu, mbar_wait(bar_group, group_phase & 1u, wc));
-            ++group_phase;
-            return r;
-        };
         for (int n = 0; n < NT; ++n, qi.next()) {
+            const int s = n % CF::kStages;
             const int q0 = qi.q_start();
-            const int q_end = qi.chunk_end();
-            const int buf = n & 1;
-            // Stage this tile's per-query LSE (base 2) and D.  Queries past
-            // the chunk end get LSE = +inf, i.e. P = 0.
-            {
-                const int qq = tid & 127;
-                const int qpos = q0 + qq;
-                const bool valid = qpos < q_end;
-                const size_t gi = (size_t)bh * p.S + (size_t)(valid ? qpos : 0);
-                if (tid < 128)
-                    row_lse2[buf * kBQ + qq] = valid ? p.lse2[gi] : INFINITY;
-                else
-                    row_D[buf * kBQ + qq] = valid ? p.Dvec[gi] : 0.f;
+            const int qcol0 = q0 + 64 * half;            // position of this half's first query
+            const int q_valid = qi.chunk_end() - qcol0;  // columns < q_valid are real queries
+            const bool diag = p.causal && qi.i == chunk_j && qi.qt == kt;
+            const bool plain = key_ok && !diag && q_valid >= 64;
+            const float* lse_s = reinterpret_cast<const float*>(smem + CF::kOffRow + s * 2 * CF::kRowBytes) + 64 * half;
+            const float* d_s = lse_s + kBQ;
+            const size_t grow = (size_t)bh * p.S;
+            if constexpr (kRowTma) {
+                // the rows arrived with the Q / dO tile of this stage
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(bar_qdo_full(s), (uint32_t)(n / CF::kStages) & 1u, wc));
+                if (!ok) break;
             }
-            ok = group_sync();
-            if (!ok) break;
             ok = __all_sync(0xffffffffu, mbar_wait(bar_s_full, (uint32_t)n & 1u, wc));
             if (!ok) break;
             tc_fence_after();
-            uint32_t sv[64];
-            tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-            tmem_ld32(tS + 32u, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-            tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-            tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-            // Causal: in chunk j's own query tiles, mask query < key.
-            const bool diag = p.causal && qi.i == chunk_j && q0 + kBQ - 1 >= k0 && q0 <= k0 + kBK - 1;
-            const float* lse2 = row_lse2 + buf * kBQ + 64 * half;
             float pv[64];
+            {
+                uint32_t sv[64];
+                tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+                tmem_ld32(tS + 32u, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+                tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+                tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+                if (plain) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                float e = ex2_approx(fmaf(__uint_as_float(sv[c]), sl2, -lse2[c]));
-                if (diag && q0 + 64 * half + c < kpos) e = 0.f;
-                pv[c] = key_ok ? e : 0.f;
+                    for (int c4 = 0; c4 < 16; ++c4) {
+                        float4 l4;
+                        if constexpr (kRowTma) {
+                            l4 = reinterpret_cast<const float4*>(lse_s)[c4];
+                        } else {
+                            const float* g = p.lse2 + grow + qcol0 + 4 * c4;
+                            l4 = make_float4(g[0], g[1], g[2], g[3]);
+                        }
+                        pv[4 * c4 + 0] = ex2_approx(fmaf(__uint_as_float(sv[4 * c4 + 0]), sl2, -l4.x));
+                        pv[4 * c4 + 1] = ex2_approx(fmaf(__uint_as_float(sv[4 * c4 + 1]), sl2, -l4.y));
+                        pv[4 * c4 + 2] = ex2_approx(fmaf(__uint_as_float(sv[4 * c4 + 2]), sl2, -l4.z));
+                        pv[4 * c4 + 3] = ex2_approx(fmaf(__uint_as_float(sv[4 * c4 + 3]), sl2, -l4.w));
+                    }
+                } else {
+                    // masked tile: rows past the chunk, causal diagonal, or
+                    // query columns past the chunk end
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) {
+                        const bool valid = key_ok && c < q_valid && !(diag && qcol0 + c < kpos);
+                        float l;
+                        if constexpr (kRowTma) l = lse_s[c];
+                        else l = valid ? p.lse2[grow + qcol0 + c] : 0.f;
+                        const float e = ex2_approx(fmaf(__uint_as_float(sv[c]), sl2, -l));
+                        pv[c] = valid ? e : 0.f;
+                    }
+                }
             }
-            uint32_t pk[32];
+            {
+                uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
-            // Both halves must have read S before either writes P over it.
-            ok = group_sync();
-            if (!ok) break;
-            tmem_st32(tPo, pk);
+                for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
+                tmem_st32(tS, pk);   // P^T bf16 over S columns [64 half, 64 half + 32)
+            }
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar_p_ready);
@@ -372,17 +390,31 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             ok = __all_sync(0xffffffffu, mbar_wait(bar_dp_full, (uint32_t)n & 1u, wc));
             if (!ok) break;
             tc_fence_after();
-            const float* Dq = row_D + buf * kBQ + 64 * half;
+            uint32_t pk[32];
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) {
                 uint32_t dp[32];
                 tmem_ld32(tDP + 32u * c2, dp);
                 tmem_ld_wait(dp);
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const int x = 32 * c2 + 2 * c;
-                    pk[16 * c2 + c] = pack_bf16x2(pv[x] * (__uint_as_float(dp[2 * c]) - Dq[x]),
-                                                  pv[x + 1] * (__uint_as_float(dp[2 * c + 1]) - Dq[x + 1]));
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    const int x = 32 * c2 + 4 * c4;
+                    float4 d4;
+                    if constexpr (kRowTma) {
+                        d4 = reinterpret_cast<const float4*>(d_s)[x >> 2];
+                    } else {
+                        float dd[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            dd[e] = (x + e < q_valid) ? p.Dvec[grow + qcol0 + x + e] : 0.f;
+                        d4 = make_float4(dd[0], dd[1], dd[2], dd[3]);
+                    }
+                    pk[16 * c2 + 2 * c4] =
+                        pack_bf16x2(pv[x] * (__uint_as_float(dp[4 * c4]) - d4.x),
+                                    pv[x + 1] * (__uint_as_float(dp[4 * c4 + 1]) - d4.y));
+                    pk[16 * c2 + 2 * c4 + 1] =
+                        pack_bf16x2(pv[x + 2] * (__uint_as_float(dp[4 * c4 + 2]) - d4.z),
+                                    pv[x + 3] * (__uint_as_float(dp[4 * c4 + 3]) - d4.w));
                 }
             }
             // dS to shared memory as [key][query] rows, 128-byte swizzle: 16-byte
@@ -393,9 +425,7 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 *reinterpret_cast<uint4*>(ds_row + ((c ^ (kr & 7)) << 4)) =
                     make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
             fence_proxy_async_smem();
-            ok = group_sync();
-            if (!ok) break;
-            tmem_st32(tDSo, pk);
+            tmem_st32(tDP, pk);      // dS^T bf16 over dP columns [64 half, 64 half + 32)
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar_ds_ready);
@@ -403,7 +433,7 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_kv_final, 0, wc));
         if (ok) {
             tc_fence_after();
-            // warps 2-5 write dV, warps 6-9 write dK (times scale)
+            // WG1 writes dV, WG2 writes dK (times scale)
             const uint32_t tAcc = tmem_addr(tmem, quarter * 32, half == 0 ? CF::kColDV : CF::kColDK);
             const float mul = half == 0 ? 1.f : p.scale;
             __nv_bfloat16* out = (half == 0 ? p.dv : p.dk) +
@@ -429,8 +459,7 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         // -------------------------------------------------------- dQ drain
         const uint32_t quarter = (uint32_t)(warp & 3);
         const int qr = (int)quarter * 32 + lane;         // query row in the tile
-        const uint32_t tA = tmem_addr(tmem, quarter * 32, CF::kColS + 64u);
-        const uint32_t tB = tmem_addr(tmem, quarter * 32, CF::kColDP + 64u);
+        const uint32_t tQ = tmem_addr(tmem, quarter * 32, CF::kColS);
         const float sc = p.scale;
         for (int n = 0; n < NT; ++n, qi.next()) {
             const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_dq_full, (uint32_t)n & 1u, wc));
@@ -439,41 +468,29 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             const int qpos = qi.q_start() + qr;
             const bool row_ok = qpos < qi.chunk_end();
             float* dst = p.dq_acc + ((size_t)bh * p.S + (size_t)(row_ok ? qpos : 0)) * D;
-            uint32_t a[32], b[32];
-            tmem_ld32(tA, a);
-            tmem_ld32(tA + 32u, b);
-            tmem_ld_wait(a);
-            tmem_ld_wait(b);
-            if constexpr (D == 64) {
-                tc_fence_before();
-                mbar_arrive(bar_dq_free);
-            }
-            if (row_ok) {
+            // Copy the tile out of TMEM half by half (64 columns at a time);
+            // the S region is released once the last half is in registers.
 #pragma unroll
-                for (int c = 0; c < 32; c += 4)
-                    red_add_v4(dst + c, __uint_as_float(a[c]) * sc, __uint_as_float(a[c + 1]) * sc,
-                               __uint_as_float(a[c + 2]) * sc, __uint_as_float(a[c + 3]) * sc);
-#pragma unroll
-                for (int c = 0; c < 32; c += 4)
-                    red_add_v4(dst + 32 + c, __uint_as_float(b[c]) * sc, __uint_as_float(b[c + 1]) * sc,
-                               __uint_as_float(b[c + 2]) * sc, __uint_as_float(b[c + 3]) * sc);
-            }
-            if constexpr (D == 128) {
-                tmem_ld32(tB, a);
-                tmem_ld32(tB + 32u, b);
+            for (int h = 0; h < D / 64; ++h) {
+                uint32_t a[32], b[32];
+                tmem_ld32(tQ + 64u * h, a);
+                tmem_ld32(tQ + 64u * h + 32u, b);
                 tmem_ld_wait(a);
                 tmem_ld_wait(b);
-                tc_fence_before();
-                mbar_arrive(bar_dq_free);
+                if (h == D / 64 - 1) {
+                    tc_fence_before();
+                    mbar_arrive(bar_dq_free);            // the S region may be reused
+                }
                 if (row_ok) {
 #pragma unroll
                     for (int c = 0; c < 32; c += 4)
-                        red_add_v4(dst + 64 + c, __uint_as_float(a[c]) * sc, __uint_as_float(a[c + 1]) * sc,
+                        red_add_v4(dst + 64 * h + c, __uint_as_float(a[c]) * sc, __uint_as_float(a[c + 1]) * sc,
                                    __uint_as_float(a[c + 2]) * sc, __uint_as_float(a[c + 3]) * sc);
 #pragma unroll
                     for (int c = 0; c < 32; c += 4)
-                        red_add_v4(dst + 96 + c, __uint_as_float(b[c]) * sc, __uint_as_float(b[c + 1]) * sc,
-                                   __uint_as_float(b[c + 2]) * sc, __uint_as_float(b[c + 3]) * sc);
+                        red_add_v4(dst + 64 * h + 32 + c, __uint_as_float(b[c]) * sc,
+                                   __uint_as_float(b[c + 1]) * sc, __uint_as_float(b[c + 2]) * sc,
+                                   __uint_as_float(b[c + 3]) * sc);
                 }
             }
         }
@@ -501,11 +518,14 @@ inline size_t workspace_bytes(int B, int H, int S, int d)
 
 inline cudaError_t configure_kernels()
 {
-    cudaError_t e = cudaFuncSetAttribute(ring_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<64>::kSmemBytes);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(ring_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Cfg<128>::kSmemBytes);
+    cudaError_t e = cudaSuccess;
+    auto set = [&](const void* fn, int bytes) {
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    };
+    set((const void*)ring_bwd_kernel<64, true>, Cfg<64>::kSmemBytes);
+    set((const void*)ring_bwd_kernel<64, false>, Cfg<64>::kSmemBytes);
+    set((const void*)ring_bwd_kernel<128, true>, Cfg<128>::kSmemBytes);
+    set((const void*)ring_bwd_kernel<128, false>, Cfg<128>::kSmemBytes);
     return e;
 }
 
@@ -521,6 +541,7 @@ struct Launch {
     uint64_t wait_limit_ns;
     cudaStream_t stream;
     int (*encode)(CUtensorMap*, const void*, int, int, int, int);
+    int (*encode_rows)(CUtensorMap*, const float*, int, int);
 };
 
 // Zero the dQ accumulator, compute D and LSE2, run the main kernel, convert
@@ -550,10 +571,18 @@ inline int launch(const Launch& L, cudaError_t* err)
     e = cudaGetLastError();
     if (e != cudaSuccess) { *err = e; return -3; }
 
-    CUtensorMap mq, mk, mv, mdo;
+    CUtensorMap mq, mk, mv, mdo, mlse, mdv;
     const int BH = L.B * L.H;
+    const int C = L.S / L.P;
+    const bool row_tma = (C % 4) == 0;
     if (L.encode(&mq, L.q, BH, L.S, L.d, kBQ) || L.encode(&mk, L.k, BH, L.S, L.d, kBK) ||
         L.encode(&mv, L.v, BH, L.S, L.d, kBK) || L.encode(&mdo, L.dO, BH, L.S, L.d, kBQ)) {
+        *err = cudaErrorInvalidValue;
+        return -3;
+    }
+    std::memset(&mlse, 0, sizeof(mlse));
+    std::memset(&mdv, 0, sizeof(mdv));
+    if (row_tma && (L.encode_rows(&mlse, lse2, BH, L.S) || L.encode_rows(&mdv, Dvec, BH, L.S))) {
         *err = cudaErrorInvalidValue;
         return -3;
     }
@@ -565,7 +594,7 @@ inline int launch(const Launch& L, cudaError_t* err)
     prm.dv = static_cast<__nv_bfloat16*>(L.dv);
     prm.S = L.S;
     prm.P = L.P;
-    prm.C = L.S / L.P;
+    prm.C = C;
     prm.causal = L.causal;
     prm.tiles_per_chunk = (prm.C + kBK - 1) / kBK;
     prm.scale = L.scale;
@@ -575,10 +604,18 @@ inline int launch(const Launch& L, cudaError_t* err)
     const long long grid = (long long)BH * L.P * prm.tiles_per_chunk;
     {
         prof::Scope ps(prof::kBwdMain, L.stream);
-        if (L.d == 128)
-            ring_bwd_kernel<128><<<(unsigned)grid, kThreads, Cfg<128>::kSmemBytes, L.stream>>>(mq, mk, mv, mdo, prm);
-        else
-            ring_bwd_kernel<64><<<(unsigned)grid, kThreads, Cfg<64>::kSmemBytes, L.stream>>>(mq, mk, mv, mdo, prm);
+        const dim3 g((unsigned)grid), b(kThreads);
+        if (L.d == 128) {
+            if (row_tma)
+                ring_bwd_kernel<128, true><<<g, b, Cfg<128>::kSmemBytes, L.stream>>>(mq, mk, mv, mdo, mlse, mdv, prm);
+            else
+                ring_bwd_kernel<128, false><<<g, b, Cfg<128>::kSmemBytes, L.stream>>>(mq, mk, mv, mdo, mlse, mdv, prm);
+        } else {
+            if (row_tma)
+                ring_bwd_kernel<64, true><<<g, b, Cfg<64>::kSmemBytes, L.stream>>>(mq, mk, mv, mdo, mlse, mdv, prm);
+            else
+                ring_bwd_kernel<64, false><<<g, b, Cfg<64>::kSmemBytes, L.stream>>>(mq, mk, mv, mdo, mlse, mdv, prm);
+        }
         ps.done();
     }
     e = cudaGetLastError();

@@ -116,6 +116,26 @@ int make_map(CUtensorMap* map, const void* ptr, int BH, int S, int d, int rows)
     return RA_OK;
 }
 
+// 2-D map over a [B*H, S] fp32 row vector: boxes of 128 consecutive rows of
+// one head, no swizzle.  Needs S % 4 == 0 (16-byte row stride).
+int make_row_map(CUtensorMap* map, const float* ptr, int BH, int S)
+{
+    cuuint64_t dims[2] = {(cuuint64_t)S, (cuuint64_t)BH};
+    cuuint64_t strides[1] = {(cuuint64_t)S * 4};
+    cuuint32_t box[2] = {128u, 1u};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        std::snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled (rows) failed (%d)",
+                      (int)r);
+        return RA_ERR_CUDA;
+    }
+    return RA_OK;
+}
+
 // Shape checks shared by the forward and backward passes.
 int check_shape(int B, int H, int S, int d, int P, int causal, float scale)
 {
@@ -254,6 +274,9 @@ int ring_attn_bwd(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, const ra
     L.stream = static_cast<cudaStream_t>(stream);
     L.encode = [](CUtensorMap* m, const void* p, int BH, int S_, int d_, int rows) {
         return make_map(m, p, BH, S_, d_, rows);
+    };
+    L.encode_rows = [](CUtensorMap* m, const float* p, int BH, int S_) {
+        return make_row_map(m, p, BH, S_);
     };
     cudaError_t e = cudaSuccess;
     rc = ra::bwd::launch(L, &e);

@@ -354,3 +354,17 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 }
 
 }  // namespace ra
+
+namespace ra {
+
+// 2-D TMA load of a box of a tensor map (no swizzle), completing on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+}  // namespace ra

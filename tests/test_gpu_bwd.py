@@ -38,7 +38,9 @@ SMALL = [
     (1, 2, 1024, 128, 4, True),
     (1, 2, 1024, 128, 4, False),
     (2, 2, 768, 64, 3, True),
-    (1, 2, 1000, 128, 4, True),     # ragged chunk tails
+    (1, 2, 1000, 128, 4, True),     # ragged chunk tails (C = 250: rows read from global)
+    (1, 2, 1200, 128, 4, True),     # ragged tails with C % 4 == 0 (C = 300: rows by TMA)
+    (1, 1, 1200, 64, 3, False),     # C = 400
     (1, 1, 1000, 64, 8, False),     # chunks shorter than a tile
     (1, 1, 384, 128, 1, True),      # P = 1
     (1, 1, 200, 128, 8, True),
