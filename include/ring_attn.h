@@ -109,6 +109,43 @@ int ring_attn_bwd(const ra_bf16 *q, const ra_bf16 *k, const ra_bf16 *v, const ra
                   size_t workspace_bytes, void *stream);
 
 /*
+ * Size of the fixed device scratch used by ring_attn_bwd_noalloc: 64 MiB per
+ * device (one copy on every GPU that loads the library, kept until the
+ * process exits).
+ */
+#define RING_ATTN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * Backward pass for callers that cannot allocate device memory -- for
+ * example code running inside a host framework that hands out all device
+ * memory through its own pool and forbids raw cudaMalloc, or code on a path
+ * where cudaMalloc / cudaFree would block or synchronize the device.  The
+ * paper has no counterpart to this entry point.
+ *
+ * Same arguments, results and errors as ring_attn_bwd, without the
+ * workspace: the fp32 dQ accumulator and the two row vectors live in a
+ * fixed static device array inside the library
+ * (RING_ATTN_NOALLOC_SCRATCH_BYTES).  The caller still passes every input
+ * and output.  Shapes whose workspace (ring_attn_bwd_workspace_size) is
+ * larger than that array return RA_ERR_UNSUPPORTED before any launch; with
+ * d = 128 the limit is about 129,000 rows of B * H * S (16 heads of 8,064
+ * tokens fit; 32 heads of 4,096 tokens do not).  The call allocates no device memory and calls
+ * no allocating library routine; it clears on `stream` the part of the
+ * scratch that must start at zero.
+ *
+ * Every call on a device shares the one array, and the array keeps the last
+ * call's contents.  Calls whose work can overlap on the GPU (for example on
+ * two streams with no ordering between them) race on it and give wrong
+ * results; order them, e.g. on one stream.  The first call on each device
+ * looks up the array's device address (with that device current); make that
+ * first call before any stream capture.
+ */
+int ring_attn_bwd_noalloc(const ra_bf16 *q, const ra_bf16 *k, const ra_bf16 *v, const ra_bf16 *o,
+                          const float *lse, const ra_bf16 *dO, ra_bf16 *dq, ra_bf16 *dk,
+                          ra_bf16 *dv, int B, int H, int S, int d, int P, int causal, float scale,
+                          void *stream);
+
+/*
  * Log-sum-exp merge of two partial attention results of the same query rows
  * (the merge each ring step performs; "Context Parallelism" guide, section
  * 2: partial results are merged with the online-softmax statistics):

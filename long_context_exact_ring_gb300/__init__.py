@@ -26,6 +26,8 @@ from ._binding import (  # noqa: F401
     profile_read,
     profile_reset,
     ring_attn_bwd,
+    ring_attn_bwd_noalloc,
+    NOALLOC_SCRATCH_BYTES,
     ring_attn_fwd,
     ring_schedule,
     set_wait_limit_ns,

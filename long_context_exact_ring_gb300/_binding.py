@@ -28,6 +28,7 @@ EXPORTED = (
     "ring_attn_fwd",
     "ring_attn_bwd_workspace_size",
     "ring_attn_bwd",
+    "ring_attn_bwd_noalloc",
     "attn_merge_partials",
     "ring_attn_schedule",
     "ring_attn_check_status",
@@ -71,6 +72,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.ring_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f,
                                       vp, sz, vp]
         lib.ring_attn_bwd.restype = i
+        lib.ring_attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i,
+                                              f, vp]
+        lib.ring_attn_bwd_noalloc.restype = i
         lib.attn_merge_partials.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, vp]
         lib.attn_merge_partials.restype = i
         lib.ring_attn_schedule.argtypes = [i, i, i, ip, ip, i]
@@ -186,6 +190,33 @@ def ring_attn_bwd(q, k, v, o, lse, dO, P: int, causal: bool, scale: float | None
                                       float(scale), workspace.data_ptr(), workspace.numel(),
                                       _stream(stream))
     _check(rc, "ring_attn_bwd")
+    return dq, dk, dv
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def ring_attn_bwd_noalloc(q, k, v, o, lse, dO, P: int, causal: bool, scale: float | None = None,
+                          *, dq, dk, dv, stream=None):
+    """ring_attn_bwd for callers that cannot allocate device memory: the
+    library's fixed static scratch replaces the workspace, and the caller
+    passes preallocated dq, dk, dv.  Calls that overlap on the GPU race on
+    the shared scratch."""
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, S, d]")
+    B, H, S, d = q.shape
+    for t, n in ((k, "k"), (v, "v"), (o, "o"), (dO, "dO"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _need(t, n, torch.bfloat16, q.shape)
+    _need(lse, "lse", torch.float32, (B, H, S))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    rc = load_library().ring_attn_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                              o.data_ptr(), lse.data_ptr(), dO.data_ptr(),
+                                              dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, S,
+                                              d, int(P), int(bool(causal)), float(scale),
+                                              _stream(stream))
+    _check(rc, "ring_attn_bwd_noalloc")
     return dq, dk, dv
 
 

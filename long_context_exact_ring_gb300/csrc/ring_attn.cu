@@ -148,6 +148,36 @@ int check_shape(int B, int H, int S, int d, int P, int causal, float scale)
     return RA_OK;
 }
 
+// Scratch of ring_attn_bwd_noalloc, for callers that cannot allocate:
+// the backward workspace (fp32 dQ accumulator, D and LSE2 rows) in static
+// device memory, one copy per device that loads the library.  Host code
+// must not pass the symbol itself to a kernel (on the host it names a
+// stand-in, not the device array); it uses the address that
+// cudaGetSymbolAddress returns for the current device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[RING_ATTN_NOALLOC_SCRATCH_BYTES];
+
+void* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device with that device current.
+int noalloc_scratch(void** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return RA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress((void**)&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(noalloc scratch)");
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return RA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -282,6 +312,21 @@ int ring_attn_bwd(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, const ra
     rc = ra::bwd::launch(L, &e);
     if (rc == RA_ERR_CUDA) return fail_cuda(e, "ring_bwd launch");
     return rc;
+}
+
+int ring_attn_bwd_noalloc(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, const ra_bf16* o,
+                          const float* lse, const ra_bf16* dO, ra_bf16* dq, ra_bf16* dk, ra_bf16* dv,
+                          int B, int H, int S, int d, int P, int causal, float scale, void* stream)
+{
+    int rc = check_shape(B, H, S, d, P, causal, scale);
+    if (rc != RA_OK) return rc;
+    if ((long long)B * H * S == 0) return RA_OK;
+    if (ra::bwd::workspace_bytes(B, H, S, d) > RING_ATTN_NOALLOC_SCRATCH_BYTES) return RA_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    rc = noalloc_scratch(&scratch);
+    if (rc != RA_OK) return rc;
+    return ring_attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, S, d, P, causal, scale, scratch,
+                         RING_ATTN_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 int attn_merge_partials(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b,
