@@ -23,21 +23,21 @@
 //   dQ_t = dS K       [queries x d]     -> TMEM S    A = dS (smem, MN-major), B = K (MN-major)
 //   dK  += dS^T Q     [keys x d]         A = dS^T (bf16 in TMEM), B = Q (MN-major)
 // TMEM (512 columns): S [0,128), dP [128,256), dV [256,256+D), dK after it.
-// Softmax warpgroup h (query columns 64h..64h+63) writes its bf16 P^T over
-// S columns [64h, 64h+32) and its dS^T over dP columns [64h, 64h+32) --
-// only columns it has read itself, so the two warpgroups never wait on each
+// Softmax warpgroup g (query columns 32g..32g+31) writes its bf16 P^T over
+// S columns [32g, 32g+16) and its dS^T over dP columns [32g, 32g+16) --
+// only columns it has read itself, so the warpgroups never wait on each
 // other.  The dQ tile reuses the whole S region once dV has consumed P^T
-// (tcgen05 MMAs of a CTA run in issue order); four drain warps copy it out
-// of TMEM while dK runs and reduce it into the fp32 dQ accumulator in global
-// memory, and the next S^T waits only for that copy.
+// (tcgen05 MMAs of a CTA run in issue order); the same warps copy it out of
+// TMEM while dK runs (warp of lane quarter q, warpgroup g: queries
+// 32q..32q+31, d columns [g D/4, (g+1) D/4)), release the region, and reduce
+// their part into the fp32 dQ accumulator in global memory.
 //
-// CTA layout (512 threads, four warpgroups):
-//   WG0  warp 0 TMA producer (K, V once; Q, dO, LSE2, D tiles in ring order),
-//        warp 1 TMEM allocator and MMA issuer, warps 2-3 idle.
-//   WG1  P^T / dS^T for query columns 0..63 (thread = key row); epilogue dV.
-//   WG2  the same for columns 64..127; epilogue dK.
-//   WG3  dQ drain (thread = query row).
-// Registers: 128 per thread (512 threads, one CTA per SM).
+// CTA layout (640 threads, five warpgroups):
+//   WG0    warp 0 TMA producer (K, V once; Q, dO, LSE2, D tiles in ring
+//          order), warp 1 TMEM allocator and MMA issuer, warps 2-3 idle.
+//   WG1-4  P^T / dS^T / dQ drain for query columns 32(g-1)..32(g-1)+31
+//          (thread = key row for P and dS, = query row for dQ); epilogue:
+//          WG1-2 write dV, WG3-4 write dK (each half of the d columns).
 #pragma once
 
 #include <cstring>
@@ -51,7 +51,8 @@ namespace bwd {
 
 constexpr int kBK = 128;        // keys per CTA
 constexpr int kBQ = 128;        // queries per streamed tile
-constexpr int kThreads = 512;
+constexpr int kThreads = 640;
+constexpr int kSoftmaxThreads = 512;   // WG1-WG4
 
 template <int D>
 struct Cfg {
@@ -178,10 +179,10 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         }
         mbar_init(bar_s_full, 1);
         mbar_init(bar_dp_full, 1);
-        mbar_init(bar_p_ready, 256);
-        mbar_init(bar_ds_ready, 256);
+        mbar_init(bar_p_ready, kSoftmaxThreads);
+        mbar_init(bar_ds_ready, kSoftmaxThreads);
         mbar_init(bar_dq_full, 1);
-        mbar_init(bar_dq_free, 128);
+        mbar_init(bar_dq_free, kSoftmaxThreads);
         mbar_init(bar_kv_final, 1);
         mbar_init(bar_drain, 1);
         fence_mbar_init();
@@ -261,12 +262,12 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                                 sdesc_sw128(sb + off, 16, 1024), idesc_kq, kk > 0 ? 1u : 0u);
                 }
             };
-            // C += A(TMEM bf16: query columns 0..63 at a_tmem, 64..127 at
-            // a_tmem + 64) * B(smem, queries x D, MN-major).
+            // C += A(TMEM bf16: queries 32g..32g+31 at columns a_tmem + 32g,
+            // 16 columns each) * B(smem, queries x D, MN-major).
             auto mma_ts = [&](uint32_t d_tmem, uint32_t a_tmem, uint32_t sb, bool first) {
 #pragma unroll
                 for (int kk = 0; kk < kBQ / 16; ++kk)
-                    mma_bf16_ts(d_tmem, a_tmem + (kk >> 2) * 64u + 8u * (kk & 3),
+                    mma_bf16_ts(d_tmem, a_tmem + (kk >> 1) * 32u + 8u * (kk & 1),
                                 sdesc_sw128(sb + kk * 2048, CF::kBoxBytes, 1024), idesc_kd,
                                 (first && kk == 0) ? 0u : 1u);
             };
@@ -311,25 +312,28 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             drain.abort_flag = &dummy;
             mbar_wait(bar_drain, 0, drain);
         }
-    } else if (wg <= 2) {
-        // ------------------------------------ P^T, dS^T; epilogue dV / dK
-        const int half = wg - 1;                         // query columns [64 half, +64)
+    } else {
+        // -------------------- P^T, dS^T, dQ drain; epilogue dV / dK
+        const int g = wg - 1;                            // query columns [32 g, 32 g + 32)
         const uint32_t quarter = (uint32_t)(warp & 3);
-        const int kr = (int)quarter * 32 + lane;         // key row in the tile
+        const int kr = (int)quarter * 32 + lane;         // key row (P, dS) / query row (dQ)
         const int kpos = k0 + kr;
         const bool key_ok = kpos < k_end;
-        const uint32_t tS = tmem_addr(tmem, quarter * 32, CF::kColS + 64u * half);
-        const uint32_t tDP = tmem_addr(tmem, quarter * 32, CF::kColDP + 64u * half);
+        const uint32_t tS = tmem_addr(tmem, quarter * 32, CF::kColS + 32u * g);
+        const uint32_t tDP = tmem_addr(tmem, quarter * 32, CF::kColDP + 32u * g);
+        constexpr int kDqCols = D / 4;                   // dQ columns this warp drains
+        const uint32_t tQ = tmem_addr(tmem, quarter * 32, CF::kColS + (uint32_t)(kDqCols * g));
         const float sl2 = p.scale_log2;
+        const float sc = p.scale;
         bool ok = true;
         for (int n = 0; n < NT; ++n, qi.next()) {
             const int s = n % CF::kStages;
             const int q0 = qi.q_start();
-            const int qcol0 = q0 + 64 * half;            // position of this half's first query
+            const int qcol0 = q0 + 32 * g;               // position of this group's first query
             const int q_valid = qi.chunk_end() - qcol0;  // columns < q_valid are real queries
             const bool diag = p.causal && qi.i == chunk_j && qi.qt == kt;
-            const bool plain = key_ok && !diag && q_valid >= 64;
-            const float* lse_s = reinterpret_cast<const float*>(smem + CF::kOffRow + s * 2 * CF::kRowBytes) + 64 * half;
+            const bool plain = key_ok && !diag && q_valid >= 32;
+            const float* lse_s = reinterpret_cast<const float*>(smem + CF::kOffRow + s * 2 * CF::kRowBytes) + 32 * g;
             const float* d_s = lse_s + kBQ;
             const size_t grow = (size_t)bh * p.S;
             if constexpr (kRowTma) {
@@ -341,22 +345,20 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             ok = __all_sync(0xffffffffu, mbar_wait(bar_s_full, (uint32_t)n & 1u, wc));
             if (!ok) break;
             tc_fence_after();
-            float pv[64];
+            float pv[32];
             {
-                uint32_t sv[64];
-                tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-                tmem_ld32(tS + 32u, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-                tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-                tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+                uint32_t sv[32];
+                tmem_ld32(tS, sv);
+                tmem_ld_wait(sv);
                 if (plain) {
 #pragma unroll
-                    for (int c4 = 0; c4 < 16; ++c4) {
+                    for (int c4 = 0; c4 < 8; ++c4) {
                         float4 l4;
                         if constexpr (kRowTma) {
                             l4 = reinterpret_cast<const float4*>(lse_s)[c4];
                         } else {
-                            const float* g = p.lse2 + grow + qcol0 + 4 * c4;
-                            l4 = make_float4(g[0], g[1], g[2], g[3]);
+                            const float* gp = p.lse2 + grow + qcol0 + 4 * c4;
+                            l4 = make_float4(gp[0], gp[1], gp[2], gp[3]);
                         }
                         pv[4 * c4 + 0] = ex2_approx(fmaf(__uint_as_float(sv[4 * c4 + 0]), sl2, -l4.x));
                         pv[4 * c4 + 1] = ex2_approx(fmaf(__uint_as_float(sv[4 * c4 + 1]), sl2, -l4.y));
@@ -367,7 +369,7 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                     // masked tile: rows past the chunk, causal diagonal, or
                     // query columns past the chunk end
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) {
+                    for (int c = 0; c < 32; ++c) {
                         const bool valid = key_ok && c < q_valid && !(diag && qcol0 + c < kpos);
                         float l;
                         if constexpr (kRowTma) l = lse_s[c];
@@ -378,10 +380,10 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 }
             }
             {
-                uint32_t pk[32];
+                uint32_t pk[16];
 #pragma unroll
-                for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
-                tmem_st32(tS, pk);   // P^T bf16 over S columns [64 half, 64 half + 32)
+                for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
+                tmem_st16(tS, pk);   // P^T bf16 over S columns [32 g, 32 g + 16)
             }
             tmem_st_wait();
             tc_fence_before();
@@ -390,18 +392,17 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             ok = __all_sync(0xffffffffu, mbar_wait(bar_dp_full, (uint32_t)n & 1u, wc));
             if (!ok) break;
             tc_fence_after();
-            uint32_t pk[32];
-#pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
+            uint32_t pk[16];
+            {
                 uint32_t dp[32];
-                tmem_ld32(tDP + 32u * c2, dp);
+                tmem_ld32(tDP, dp);
                 tmem_ld_wait(dp);
 #pragma unroll
                 for (int c4 = 0; c4 < 8; ++c4) {
-                    const int x = 32 * c2 + 4 * c4;
+                    const int x = 4 * c4;
                     float4 d4;
                     if constexpr (kRowTma) {
-                        d4 = reinterpret_cast<const float4*>(d_s)[x >> 2];
+                        d4 = reinterpret_cast<const float4*>(d_s)[c4];
                     } else {
                         float dd[4];
 #pragma unroll
@@ -409,88 +410,73 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                             dd[e] = (x + e < q_valid) ? p.Dvec[grow + qcol0 + x + e] : 0.f;
                         d4 = make_float4(dd[0], dd[1], dd[2], dd[3]);
                     }
-                    pk[16 * c2 + 2 * c4] =
-                        pack_bf16x2(pv[x] * (__uint_as_float(dp[4 * c4]) - d4.x),
-                                    pv[x + 1] * (__uint_as_float(dp[4 * c4 + 1]) - d4.y));
-                    pk[16 * c2 + 2 * c4 + 1] =
-                        pack_bf16x2(pv[x + 2] * (__uint_as_float(dp[4 * c4 + 2]) - d4.z),
-                                    pv[x + 3] * (__uint_as_float(dp[4 * c4 + 3]) - d4.w));
+                    pk[2 * c4] = pack_bf16x2(pv[x] * (__uint_as_float(dp[x]) - d4.x),
+                                             pv[x + 1] * (__uint_as_float(dp[x + 1]) - d4.y));
+                    pk[2 * c4 + 1] = pack_bf16x2(pv[x + 2] * (__uint_as_float(dp[x + 2]) - d4.z),
+                                                 pv[x + 3] * (__uint_as_float(dp[x + 3]) - d4.w));
                 }
             }
-            // dS to shared memory as [key][query] rows, 128-byte swizzle: 16-byte
-            // chunk c of row kr sits at chunk position c ^ (kr & 7).
-            uint8_t* ds_row = smem + CF::kOffDS + half * CF::kBoxBytes + kr * 128;
+            // dS to shared memory as [key][query] rows, 128-byte swizzle: the
+            // 16-byte chunk c of row kr sits at chunk position c ^ (kr & 7);
+            // this group's 32 queries are chunks 4 (g & 1) .. +3 of atom g / 2.
+            uint8_t* ds_row = smem + CF::kOffDS + (g >> 1) * CF::kBoxBytes + kr * 128;
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4*>(ds_row + ((c ^ (kr & 7)) << 4)) =
+            for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<uint4*>(ds_row + (((4 * (g & 1) + c) ^ (kr & 7)) << 4)) =
                     make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
             fence_proxy_async_smem();
-            tmem_st32(tDP, pk);      // dS^T bf16 over dP columns [64 half, 64 half + 32)
+            tmem_st16(tDP, pk);      // dS^T bf16 over dP columns [32 g, 32 g + 16)
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar_ds_ready);
+
+            // dQ drain: this warp's query rows, d columns [g D/4, (g+1) D/4)
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_dq_full, (uint32_t)n & 1u, wc));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t a[kDqCols];
+            if constexpr (kDqCols == 32) {
+                tmem_ld32(tQ, *reinterpret_cast<uint32_t(*)[32]>(&a[0]));
+                tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&a[0]));
+            } else {
+                tmem_ld16(tQ, *reinterpret_cast<uint32_t(*)[16]>(&a[0]));
+                tmem_ld_wait16(*reinterpret_cast<uint32_t(*)[16]>(&a[0]));
+            }
+            tc_fence_before();
+            mbar_arrive(bar_dq_free);                    // the S region may be reused
+            const int qpos = q0 + kr;
+            if (qpos < qi.chunk_end()) {
+                float* dst = p.dq_acc + ((size_t)bh * p.S + (size_t)qpos) * D + kDqCols * g;
+#pragma unroll
+                for (int c = 0; c < kDqCols; c += 4)
+                    red_add_v4(dst + c, __uint_as_float(a[c]) * sc, __uint_as_float(a[c + 1]) * sc,
+                               __uint_as_float(a[c + 2]) * sc, __uint_as_float(a[c + 3]) * sc);
+            }
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_kv_final, 0, wc));
         if (ok) {
             tc_fence_after();
-            // WG1 writes dV, WG2 writes dK (times scale)
-            const uint32_t tAcc = tmem_addr(tmem, quarter * 32, half == 0 ? CF::kColDV : CF::kColDK);
-            const float mul = half == 0 ? 1.f : p.scale;
-            __nv_bfloat16* out = (half == 0 ? p.dv : p.dk) +
-                                 ((size_t)bh * p.S + (size_t)(key_ok ? kpos : 0)) * D;
+            // WG1-2 write dV, WG3-4 write dK (times scale); each half of d
+            const bool is_dk = g >= 2;
+            const int col0 = (g & 1) * (D / 2);
+            const uint32_t tAcc = tmem_addr(tmem, quarter * 32, (is_dk ? CF::kColDK : CF::kColDV) + col0);
+            const float mul = is_dk ? p.scale : 1.f;
+            __nv_bfloat16* out = (is_dk ? p.dk : p.dv) +
+                                 ((size_t)bh * p.S + (size_t)(key_ok ? kpos : 0)) * D + col0;
 #pragma unroll
-            for (int c4 = 0; c4 < D / 32; ++c4) {
-                uint32_t a[32];
-                tmem_ld32(tAcc + 32u * c4, a);
-                tmem_ld_wait(a);
+            for (int c4 = 0; c4 < D / 64; ++c4) {
+                uint32_t acc[32];
+                tmem_ld32(tAcc + 32u * c4, acc);
+                tmem_ld_wait(acc);
                 uint32_t o16[16];
 #pragma unroll
                 for (int c = 0; c < 16; ++c)
-                    o16[c] = pack_bf16x2(__uint_as_float(a[2 * c]) * mul, __uint_as_float(a[2 * c + 1]) * mul);
+                    o16[c] = pack_bf16x2(__uint_as_float(acc[2 * c]) * mul, __uint_as_float(acc[2 * c + 1]) * mul);
                 if (key_ok) {
                     uint4* dst = reinterpret_cast<uint4*>(out + 32 * c4);
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4)
                         dst[v4] = make_uint4(o16[4 * v4], o16[4 * v4 + 1], o16[4 * v4 + 2], o16[4 * v4 + 3]);
-                }
-            }
-        }
-    } else {
-        // -------------------------------------------------------- dQ drain
-        const uint32_t quarter = (uint32_t)(warp & 3);
-        const int qr = (int)quarter * 32 + lane;         // query row in the tile
-        const uint32_t tQ = tmem_addr(tmem, quarter * 32, CF::kColS);
-        const float sc = p.scale;
-        for (int n = 0; n < NT; ++n, qi.next()) {
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_dq_full, (uint32_t)n & 1u, wc));
-            if (!ok) break;
-            tc_fence_after();
-            const int qpos = qi.q_start() + qr;
-            const bool row_ok = qpos < qi.chunk_end();
-            float* dst = p.dq_acc + ((size_t)bh * p.S + (size_t)(row_ok ? qpos : 0)) * D;
-            // Copy the tile out of TMEM half by half (64 columns at a time);
-            // the S region is released once the last half is in registers.
-#pragma unroll
-            for (int h = 0; h < D / 64; ++h) {
-                uint32_t a[32], b[32];
-                tmem_ld32(tQ + 64u * h, a);
-                tmem_ld32(tQ + 64u * h + 32u, b);
-                tmem_ld_wait(a);
-                tmem_ld_wait(b);
-                if (h == D / 64 - 1) {
-                    tc_fence_before();
-                    mbar_arrive(bar_dq_free);            // the S region may be reused
-                }
-                if (row_ok) {
-#pragma unroll
-                    for (int c = 0; c < 32; c += 4)
-                        red_add_v4(dst + 64 * h + c, __uint_as_float(a[c]) * sc, __uint_as_float(a[c + 1]) * sc,
-                                   __uint_as_float(a[c + 2]) * sc, __uint_as_float(a[c + 3]) * sc);
-#pragma unroll
-                    for (int c = 0; c < 32; c += 4)
-                        red_add_v4(dst + 64 * h + 32 + c, __uint_as_float(b[c]) * sc,
-                                   __uint_as_float(b[c + 1]) * sc, __uint_as_float(b[c + 2]) * sc,
-                                   __uint_as_float(b[c + 3]) * sc);
                 }
             }
         }
