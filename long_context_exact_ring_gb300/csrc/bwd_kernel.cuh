@@ -29,12 +29,16 @@
 // other.  The dQ tile reuses the whole S region once dV has consumed P^T
 // (tcgen05 MMAs of a CTA run in issue order); the same warps copy it out of
 // TMEM while dK runs (warp of lane quarter q, warpgroup g: queries
-// 32q..32q+31, d columns [g D/4, (g+1) D/4)), release the region, and reduce
-// their part into the fp32 dQ accumulator in global memory.
+// 32q..32q+31, d columns [g D/4, (g+1) D/4)) and release the region.  Once
+// dK has consumed the tile's Q / dO stage, they write the scaled fp32 tile
+// into that stage's buffers (128-byte swizzled boxes of 32 columns), and one
+// thread adds it to the fp32 dQ accumulator in global memory with a few TMA
+// bulk reduce-adds before handing the stage back to the producer.
 //
 // CTA layout (640 threads, five warpgroups):
 //   WG0    warp 0 TMA producer (K, V once; Q, dO, LSE2, D tiles in ring
-//          order), warp 1 TMEM allocator and MMA issuer, warps 2-3 idle.
+//          order), warp 1 TMEM allocator and MMA issuer, warp 2 dQ reducer
+//          (TMA reduce-add of the staged dQ tiles), warp 3 idle.
 //   WG1-4  P^T / dS^T / dQ drain for query columns 32(g-1)..32(g-1)+31
 //          (thread = key row for P and dS, = query row for dQ); epilogue:
 //          WG1-2 write dV, WG3-4 write dK (each half of the d columns).
@@ -124,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                 const __grid_constant__ CUtensorMap map_lse2, const __grid_constant__ CUtensorMap map_dvec,
-                const BwdParams p)
+                const __grid_constant__ CUtensorMap map_dq, const BwdParams p)
 {
     using CF = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -151,6 +155,8 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     const uint32_t bar_dq_free = bar0 + 8u * 10;
     const uint32_t bar_kv_final = bar0 + 8u * 11;
     const uint32_t bar_drain = bar0 + 8u * 12;
+    const uint32_t bar_k_done = bar0 + 8u * 13;     // dK of the tile done: its Q / dO stage is readable scratch
+    const uint32_t bar_dq_staged = bar0 + 8u * 14;  // the tile's dQ sits in that stage
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + CF::kOffBar + 192);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + CF::kOffBar + 200);
 
@@ -185,6 +191,8 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         mbar_init(bar_dq_free, kSoftmaxThreads);
         mbar_init(bar_kv_final, 1);
         mbar_init(bar_drain, 1);
+        mbar_init(bar_k_done, 1);
+        mbar_init(bar_dq_staged, kSoftmaxThreads);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -303,7 +311,7 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                                 kk > 0 ? 1u : 0u);
                 mma_commit(bar_dq_full);
                 mma_ts(tmem + CF::kColDK, tmem + CF::kColDP, qs, n == 0);
-                mma_commit(bar_qdo_empty(s));
+                mma_commit(bar_k_done);
             }
             if (ok) mma_commit(bar_kv_final);
             mma_commit(bar_drain);
@@ -311,6 +319,29 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             volatile int dummy = 0;
             drain.abort_flag = &dummy;
             mbar_wait(bar_drain, 0, drain);
+        } else if (warp == 2 && lane == 0) {
+            // ---------------------------------------------------- dQ reducer
+            // For each tile: wait until its dQ is staged in the stage's Q /
+            // dO buffers, add the D / 32 boxes [128 rows x 32 columns] to the
+            // fp32 accumulator, and free the stage once the bulk copies have
+            // read it.  Rows past S are skipped by the TMA; rows past the
+            // chunk end hold exact zeros (their P is masked to 0).
+            tma_prefetch_desc(&map_dq);
+            for (int n = 0; n < NT; ++n, qi.next()) {
+                const int s = n % CF::kStages;
+                if (!mbar_wait(bar_dq_staged, (uint32_t)n & 1u, wc)) break;
+                const int q0 = qi.q_start();
+#pragma unroll
+                for (int b = 0; b < D / 32; ++b) {
+                    const uint32_t src = (b < D / 64 ? sQ : sDO) + s * CF::kTileBytes +
+                                         (b % (D / 64)) * CF::kBoxBytes;
+                    tma_reduce_add_3d(&map_dq, src, 32 * b, q0, bh);
+                }
+                bulk_commit_group();
+                bulk_wait_read_all();
+                mbar_arrive(bar_qdo_empty(s));
+            }
+            bulk_wait_all();
         }
     } else {
         // -------------------- P^T, dS^T, dQ drain; epilogue dV / dK
@@ -444,14 +475,26 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             }
             tc_fence_before();
             mbar_arrive(bar_dq_free);                    // the S region may be reused
-            const int qpos = q0 + kr;
-            if (qpos < qi.chunk_end()) {
-                float* dst = p.dq_acc + ((size_t)bh * p.S + (size_t)qpos) * D + kDqCols * g;
+            // Stage the scaled values in this tile's Q / dO buffers once dK
+            // has read them: box b = (kDqCols g) / 32 holds d columns
+            // [32 b, 32 b + 32) as [128 rows][128 bytes], 16-byte chunk c of
+            // row kr at chunk position c ^ (kr & 7).
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_k_done, (uint32_t)n & 1u, wc));
+            if (!ok) break;
+            {
+                constexpr int kBoxesQ = D / 64;          // boxes in the Q buffer
+                const int b = (kDqCols * g) / 32;
+                const int c_first = ((kDqCols * g) % 32) / 4;
+                uint8_t* box = smem + (b < kBoxesQ ? CF::kOffQ : CF::kOffDO) + s * CF::kTileBytes +
+                               (b % kBoxesQ) * CF::kBoxBytes + kr * 128;
 #pragma unroll
-                for (int c = 0; c < kDqCols; c += 4)
-                    red_add_v4(dst + c, __uint_as_float(a[c]) * sc, __uint_as_float(a[c + 1]) * sc,
-                               __uint_as_float(a[c + 2]) * sc, __uint_as_float(a[c + 3]) * sc);
+                for (int c = 0; c < kDqCols / 4; ++c)
+                    *reinterpret_cast<float4*>(box + (((c_first + c) ^ (kr & 7)) << 4)) =
+                        make_float4(__uint_as_float(a[4 * c]) * sc, __uint_as_float(a[4 * c + 1]) * sc,
+                                    __uint_as_float(a[4 * c + 2]) * sc, __uint_as_float(a[4 * c + 3]) * sc);
             }
+            fence_proxy_async_smem();
+            mbar_arrive(bar_dq_staged);
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_kv_final, 0, wc));
         if (ok) {
@@ -528,6 +571,7 @@ struct Launch {
     cudaStream_t stream;
     int (*encode)(CUtensorMap*, const void*, int, int, int, int);
     int (*encode_rows)(CUtensorMap*, const float*, int, int);
+    int (*encode_acc)(CUtensorMap*, float*, int, int, int);
 };
 
 // Zero the dQ accumulator, compute D and LSE2, run the main kernel, convert
@@ -557,12 +601,16 @@ inline int launch(const Launch& L, cudaError_t* err)
     e = cudaGetLastError();
     if (e != cudaSuccess) { *err = e; return -3; }
 
-    CUtensorMap mq, mk, mv, mdo, mlse, mdv;
+    CUtensorMap mq, mk, mv, mdo, mlse, mdv, mdq;
     const int BH = L.B * L.H;
     const int C = L.S / L.P;
     const bool row_tma = (C % 4) == 0;
     if (L.encode(&mq, L.q, BH, L.S, L.d, kBQ) || L.encode(&mk, L.k, BH, L.S, L.d, kBK) ||
         L.encode(&mv, L.v, BH, L.S, L.d, kBK) || L.encode(&mdo, L.dO, BH, L.S, L.d, kBQ)) {
+        *err = cudaErrorInvalidValue;
+        return -3;
+    }
+    if (L.encode_acc(&mdq, dq_acc, BH, L.S, L.d)) {
         *err = cudaErrorInvalidValue;
         return -3;
     }
@@ -593,14 +641,14 @@ inline int launch(const Launch& L, cudaError_t* err)
         const dim3 g((unsigned)grid), b(kThreads);
         if (L.d == 128) {
             if (row_tma)
-                ring_bwd_kernel<128, true><<<g, b, Cfg<128>::kSmemBytes, L.stream>>>(mq, mk, mv, mdo, mlse, mdv, prm);
+                ring_bwd_kernel<128, true><<<g, b, Cfg<128>::kSmemBytes, L.stream>>>(mq, mk, mv, mdo, mlse, mdv, mdq, prm);
             else
-                ring_bwd_kernel<128, false><<<g, b, Cfg<128>::kSmemBytes, L.stream>>>(mq, mk, mv, mdo, mlse, mdv, prm);
+                ring_bwd_kernel<128, false><<<g, b, Cfg<128>::kSmemBytes, L.stream>>>(mq, mk, mv, mdo, mlse, mdv, mdq, prm);
         } else {
             if (row_tma)
-                ring_bwd_kernel<64, true><<<g, b, Cfg<64>::kSmemBytes, L.stream>>>(mq, mk, mv, mdo, mlse, mdv, prm);
+                ring_bwd_kernel<64, true><<<g, b, Cfg<64>::kSmemBytes, L.stream>>>(mq, mk, mv, mdo, mlse, mdv, mdq, prm);
             else
-                ring_bwd_kernel<64, false><<<g, b, Cfg<64>::kSmemBytes, L.stream>>>(mq, mk, mv, mdo, mlse, mdv, prm);
+                ring_bwd_kernel<64, false><<<g, b, Cfg<64>::kSmemBytes, L.stream>>>(mq, mk, mv, mdo, mlse, mdv, mdq, prm);
         }
         ps.done();
     }

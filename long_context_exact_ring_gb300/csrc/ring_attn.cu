@@ -136,6 +136,26 @@ int make_row_map(CUtensorMap* map, const float* ptr, int BH, int S)
     return RA_OK;
 }
 
+// 3-D map over the fp32 dQ accumulator [B*H, S, d]: boxes of 32 columns x
+// 128 rows x 1 head with 128-byte swizzle, used for TMA reduce-adds.  Rows
+// past S are not written.
+int make_acc_map(CUtensorMap* map, float* ptr, int BH, int S, int d)
+{
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)S, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)S * d * 4};
+    cuuint32_t box[3] = {32u, 128u, 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        std::snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled (dQ) failed (%d)",
+                      (int)r);
+        return RA_ERR_CUDA;
+    }
+    return RA_OK;
+}
+
 // Shape checks shared by the forward and backward passes.
 int check_shape(int B, int H, int S, int d, int P, int causal, float scale)
 {
@@ -307,6 +327,9 @@ int ring_attn_bwd(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, const ra
     };
     L.encode_rows = [](CUtensorMap* m, const float* p, int BH, int S_) {
         return make_row_map(m, p, BH, S_);
+    };
+    L.encode_acc = [](CUtensorMap* m, float* p, int BH, int S_, int d_) {
+        return make_acc_map(m, p, BH, S_, d_);
     };
     cudaError_t e = cudaSuccess;
     rc = ra::bwd::launch(L, &e);
