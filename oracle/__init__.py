@@ -17,6 +17,9 @@ from .oracle import (  # noqa: F401
     partial,
     bwd,
     bwd_dq_rows,
+    naive_fwd_gqa,
+    naive_fwd_rows_gqa,
+    bwd_gqa,
     ring_step_bytes,
     ring_total_bytes,
     kv_cache_bytes_per_token,

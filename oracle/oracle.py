@@ -216,6 +216,46 @@ def bwd_dq_rows(q, k, v, dO, causal: bool, scale: float, rows):
 
 
 # ---------------------------------------------------------------------------
+# Grouped-query attention: H query heads share H_kv key/value heads; query
+# head h reads key/value head h // (H / H_kv).  The pages name GQA as the
+# case where ring attention, unlike head-partitioned schemes, does not depend
+# on the head count ("Training Long-Context Models Without OOM: Ring
+# Attention", section "Ring Attention vs. DeepSpeed Ulysses (All-to-All)").
+# The definition is multi-head attention on K and V with each head repeated
+# for its group; the gradient of a shared K or V head is the sum over its
+# group.
+# ---------------------------------------------------------------------------
+
+def _repeat_kv(x, H: int):
+    x = _f64(x)
+    Hkv = x.shape[1]
+    if H % Hkv:
+        raise ValueError("H must be a multiple of H_kv")
+    return np.ascontiguousarray(np.repeat(x, H // Hkv, axis=1))
+
+
+def naive_fwd_gqa(q, k, v, causal: bool, scale: float):
+    """GQA forward -> (O [B,H,S,d], LSE [B,H,S]); k, v are [B,H_kv,S,d]."""
+    H = np.asarray(q).shape[1]
+    return naive_fwd(q, _repeat_kv(k, H), _repeat_kv(v, H), causal, scale)
+
+
+def naive_fwd_rows_gqa(q, k, v, causal: bool, scale: float, rows):
+    H = np.asarray(q).shape[1]
+    return naive_fwd_rows(q, _repeat_kv(k, H), _repeat_kv(v, H), causal, scale, rows)
+
+
+def bwd_gqa(q, k, v, dO, causal: bool, scale: float):
+    """GQA backward -> (dQ [B,H,S,d], dK, dV [B,H_kv,S,d])."""
+    q = _f64(q)
+    B, H, S, d = q.shape
+    Hkv = np.asarray(k).shape[1]
+    dq, dk, dv, _, _ = bwd(q, _repeat_kv(k, H), _repeat_kv(v, H), dO, causal, scale)
+    G = H // Hkv
+    return dq, dk.reshape(B, Hkv, G, S, d).sum(axis=2), dv.reshape(B, Hkv, G, S, d).sum(axis=2)
+
+
+# ---------------------------------------------------------------------------
 # Analytic helpers ("Context Parallelism" guide, section 2)
 # ---------------------------------------------------------------------------
 

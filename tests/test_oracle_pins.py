@@ -369,3 +369,58 @@ def test_flop_count_reading():
     f = oracle.attention_flops(1, 32, 131072, 128, True)
     assert f == 4 * 128 * 32 * (131072 * 131073 // 2)
     assert abs(f - 1.4074e14) / 1.4074e14 < 1e-3
+
+
+# --------------------------------------------------------------------------
+# Grouped-query attention
+# --------------------------------------------------------------------------
+
+def test_gqa_with_one_group_member_is_mha():
+    q, k, v = _rand(1, 3, 9, 4, 51)
+    o1, l1 = oracle.naive_fwd_gqa(q, k, v, True, 0.5)
+    o2, l2 = oracle.naive_fwd(q, k, v, True, 0.5)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+def test_gqa_heads_of_a_group_see_the_same_keys():
+    # MQA (one K/V head): a query head's output depends only on its own
+    # queries and the shared K/V -- recomputing head h alone gives the same.
+    B, H, S, d = 1, 4, 7, 3
+    g = np.random.default_rng(52)
+    q = g.standard_normal((B, H, S, d))
+    k = g.standard_normal((B, 1, S, d))
+    v = g.standard_normal((B, 1, S, d))
+    o, lse = oracle.naive_fwd_gqa(q, k, v, False, 0.7)
+    for h in range(H):
+        o_h, l_h = oracle.naive_fwd(q[:, h:h + 1], k, v, False, 0.7)
+        np.testing.assert_allclose(o[:, h:h + 1], o_h, atol=1e-15)
+        np.testing.assert_allclose(lse[:, h:h + 1], l_h, atol=1e-15)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_backward_finite_differences(causal):
+    # dK, dV of a shared head collect the whole group: checked against
+    # central differences of the GQA forward.
+    B, H, Hkv, S, d = 1, 4, 2, 5, 3
+    g = np.random.default_rng(53)
+    q = g.standard_normal((B, H, S, d))
+    k = g.standard_normal((B, Hkv, S, d))
+    v = g.standard_normal((B, Hkv, S, d))
+    dO = g.standard_normal((B, H, S, d))
+    scale = 0.6
+    dq, dk, dv = oracle.bwd_gqa(q, k, v, dO, causal, scale)
+
+    def loss(q_, k_, v_):
+        o, _ = oracle.naive_fwd_gqa(q_, k_, v_, causal, scale)
+        return float((o * dO).sum())
+    eps = 1e-6
+    for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp = x.copy(); xp[idx] += eps
+            xm = x.copy(); xm[idx] -= eps
+            a = {"q": q, "k": k, "v": v}; a[name] = xp
+            b = {"q": q, "k": k, "v": v}; b[name] = xm
+            num[idx] = (loss(a["q"], a["k"], a["v"]) - loss(b["q"], b["k"], b["v"])) / (2 * eps)
+        assert np.abs(num - grad).max() / np.abs(num).max() < 1e-6, name
