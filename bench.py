@@ -283,7 +283,7 @@ def main():
     o = torch.empty_like(q)
     lse = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
     if w.backward:
-        dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         ws = torch.empty(ra.bwd_workspace_size(B, H, S, d), dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
@@ -408,7 +408,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) on device)",
-            "config": {"workload": w.name, "B": B, "H": H, "S": S, "d": d, "P": P,
+            "config": {"workload": w.name, "B": B, "H": H, "H_kv": inp["H_kv"], "S": S, "d": d, "P": P,
                        "causal": causal, "passes": "fwd+bwd" if w.backward else "fwd",
                        "l2": "inputs larger than L2 (1 GiB per tensor)",
                        "parallelism": f"replicas x{world}"},

@@ -77,6 +77,20 @@ int ring_attn_fwd(const ra_bf16 *q, const ra_bf16 *k, const ra_bf16 *v, ra_bf16 
                   int B, int H, int S, int d, int P, int causal, float scale, void *stream);
 
 /*
+ * Grouped-query forward: H query heads share H_kv key/value heads, query
+ * head h reading key/value head h / (H / H_kv) -- the case the pages single
+ * out, where ring attention does not depend on the head count ("Training
+ * Long-Context Models Without OOM: Ring Attention", section "Ring Attention
+ * vs. DeepSpeed Ulysses (All-to-All)").  q, o are [B, H, S, d]; k, v are
+ * [B, H_kv, S, d]; lse is [B, H, S].  H_kv >= 1 and H % H_kv == 0, else
+ * RA_ERR_INVALID_ARG.  Everything else as ring_attn_fwd, which is this call
+ * with H_kv = H.
+ */
+int ring_attn_fwd_gqa(const ra_bf16 *q, const ra_bf16 *k, const ra_bf16 *v, ra_bf16 *o, float *lse,
+                      int B, int H, int H_kv, int S, int d, int P, int causal, float scale,
+                      void *stream);
+
+/*
  * Bytes of device workspace ring_attn_bwd needs for this shape: an fp32 dQ
  * accumulator [B, H, S, d] plus two fp32 row vectors [B, H, S]
  * (D_r = sum dO_r * O_r and LSE in base 2), each section 256-byte aligned.
@@ -107,6 +121,17 @@ int ring_attn_bwd(const ra_bf16 *q, const ra_bf16 *k, const ra_bf16 *v, const ra
                   const float *lse, const ra_bf16 *dO, ra_bf16 *dq, ra_bf16 *dk, ra_bf16 *dv,
                   int B, int H, int S, int d, int P, int causal, float scale, void *workspace,
                   size_t workspace_bytes, void *stream);
+
+/*
+ * Grouped-query backward: shapes as ring_attn_fwd_gqa; dq is [B, H, S, d],
+ * dk and dv are [B, H_kv, S, d] and collect the gradients of every query
+ * head of their group.  The workspace is ring_attn_bwd_workspace_size(B, H,
+ * S, d) (query heads).  ring_attn_bwd is this call with H_kv = H.
+ */
+int ring_attn_bwd_gqa(const ra_bf16 *q, const ra_bf16 *k, const ra_bf16 *v, const ra_bf16 *o,
+                      const float *lse, const ra_bf16 *dO, ra_bf16 *dq, ra_bf16 *dk, ra_bf16 *dv,
+                      int B, int H, int H_kv, int S, int d, int P, int causal, float scale,
+                      void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Size of the fixed device scratch used by ring_attn_bwd_noalloc: 64 MiB per

@@ -26,6 +26,8 @@ RA_ERR_DEVICE_TIMEOUT = -4
 
 EXPORTED = (
     "ring_attn_fwd",
+    "ring_attn_fwd_gqa",
+    "ring_attn_bwd_gqa",
     "ring_attn_bwd_workspace_size",
     "ring_attn_bwd",
     "ring_attn_bwd_noalloc",
@@ -67,6 +69,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         ip = ctypes.POINTER(ctypes.c_int)
         lib.ring_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
         lib.ring_attn_fwd.restype = i
+        lib.ring_attn_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+        lib.ring_attn_fwd_gqa.restype = i
+        lib.ring_attn_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i,
+                                          f, vp, sz, vp]
+        lib.ring_attn_bwd_gqa.restype = i
         lib.ring_attn_bwd_workspace_size.argtypes = [i, i, i, i]
         lib.ring_attn_bwd_workspace_size.restype = sz
         lib.ring_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f,
@@ -135,15 +142,29 @@ def _need(t: torch.Tensor, name: str, dtype, shape=None):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
+def _kv_heads(q, k, v):
+    """H_kv from k / v shaped [B, H_kv, S, d] with H % H_kv == 0."""
+    B, H, S, d = q.shape
+    if k.dim() != 4 or k.shape[0] != B or k.shape[2:] != q.shape[2:]:
+        raise ValueError(f"k has shape {tuple(k.shape)}, expected [B, H_kv, S, d] matching q")
+    H_kv = k.shape[1]
+    if H_kv < 1 or H % H_kv:
+        raise ValueError(f"query heads ({H}) must be a multiple of key/value heads ({H_kv})")
+    _need(k, "k", torch.bfloat16, (B, H_kv, S, d))
+    _need(v, "v", torch.bfloat16, (B, H_kv, S, d))
+    return H_kv
+
+
 def ring_attn_fwd(q, k, v, P: int, causal: bool, scale: float | None = None, *,
                   o=None, lse=None, stream=None):
-    """O, LSE = exact ring attention of bf16 [B, H, S, d] q, k, v over P chunks."""
+    """O, LSE = exact ring attention of bf16 [B, H, S, d] q over P chunks.
+    k, v are [B, H_kv, S, d]; H_kv < H is grouped-query attention (query
+    head h reads key/value head h // (H / H_kv))."""
     _need(q, "q", torch.bfloat16)
     if q.dim() != 4:
         raise ValueError("q must be [B, H, S, d]")
     B, H, S, d = q.shape
-    _need(k, "k", torch.bfloat16, q.shape)
-    _need(v, "v", torch.bfloat16, q.shape)
+    H_kv = _kv_heads(q, k, v)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if o is None:
@@ -152,9 +173,15 @@ def ring_attn_fwd(q, k, v, P: int, causal: bool, scale: float | None = None, *,
         lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
     _need(o, "o", torch.bfloat16, q.shape)
     _need(lse, "lse", torch.float32, (B, H, S))
-    rc = load_library().ring_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                      lse.data_ptr(), B, H, S, d, int(P), int(bool(causal)),
-                                      float(scale), _stream(stream))
+    lib = load_library()
+    if H_kv == H:
+        rc = lib.ring_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               lse.data_ptr(), B, H, S, d, int(P), int(bool(causal)),
+                               float(scale), _stream(stream))
+    else:
+        rc = lib.ring_attn_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), B, H, H_kv, S, d, int(P), int(bool(causal)),
+                                   float(scale), _stream(stream))
     _check(rc, "ring_attn_fwd")
     return o, lse
 
@@ -165,30 +192,41 @@ def bwd_workspace_size(B: int, H: int, S: int, d: int) -> int:
 
 def ring_attn_bwd(q, k, v, o, lse, dO, P: int, causal: bool, scale: float | None = None, *,
                   dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """dQ, dK, dV of exact ring attention (P recomputed from the saved LSE)."""
+    """dQ, dK, dV of exact ring attention (P recomputed from the saved LSE).
+    With grouped-query k, v ([B, H_kv, S, d]) dk and dv have that shape."""
     _need(q, "q", torch.bfloat16)
     if q.dim() != 4:
         raise ValueError("q must be [B, H, S, d]")
     B, H, S, d = q.shape
-    for t, n in ((k, "k"), (v, "v"), (o, "o"), (dO, "dO")):
+    H_kv = _kv_heads(q, k, v)
+    for t, n in ((o, "o"), (dO, "dO")):
         _need(t, n, torch.bfloat16, q.shape)
     _need(lse, "lse", torch.float32, (B, H, S))
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
-    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
-        _need(t, n, torch.bfloat16, q.shape)
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _need(dq, "dq", torch.bfloat16, q.shape)
+    _need(dk, "dk", torch.bfloat16, k.shape)
+    _need(dv, "dv", torch.bfloat16, v.shape)
     need = bwd_workspace_size(B, H, S, d)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     _need(workspace, "workspace", torch.uint8)
-    rc = load_library().ring_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                      lse.data_ptr(), dO.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                                      dv.data_ptr(), B, H, S, d, int(P), int(bool(causal)),
-                                      float(scale), workspace.data_ptr(), workspace.numel(),
-                                      _stream(stream))
+    lib = load_library()
+    if H_kv == H:
+        rc = lib.ring_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               lse.data_ptr(), dO.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                               dv.data_ptr(), B, H, S, d, int(P), int(bool(causal)),
+                               float(scale), workspace.data_ptr(), workspace.numel(),
+                               _stream(stream))
+    else:
+        rc = lib.ring_attn_bwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), dO.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                   dv.data_ptr(), B, H, H_kv, S, d, int(P), int(bool(causal)),
+                                   float(scale), workspace.data_ptr(), workspace.numel(),
+                                   _stream(stream))
     _check(rc, "ring_attn_bwd")
     return dq, dk, dv
 

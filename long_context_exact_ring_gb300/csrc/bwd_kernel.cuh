@@ -15,6 +15,9 @@
 // tiles that meet chunk j in the ring: query chunk i = j, j+1, ... (mod P) --
 // chunk j is visited by query chunk i at ring step t = (i - j) mod P.  Causal
 // drops i < j and, inside chunk j, query tiles wholly above the diagonal.
+// With grouped-query attention the CTA streams these tiles for every query
+// head of its key/value head's group, one head after the other, so dK and dV
+// collect the whole group in TMEM.
 //
 // Per query tile, on the tensor core (bf16 x bf16 -> fp32), in issue order:
 //   S^T  = K Q^T      [keys x queries]  -> TMEM S    (A = K, B = Q, K-major)
@@ -89,6 +92,7 @@ struct BwdParams {
     __nv_bfloat16* dk;      // [B*H*S, D]
     __nv_bfloat16* dv;
     int S, P, C, causal, tiles_per_chunk;
+    int H, group;           // query heads; query heads per key/value head
     float scale, scale_log2;
     uint32_t* status;
     uint64_t wait_limit_ns;
@@ -96,24 +100,34 @@ struct BwdParams {
 
 // Query tiles met by key tile kt of chunk j, in ring order: chunks
 // i = j, j+1, ... (mod P), each chunk's tiles ascending; causal keeps
-// i >= j and, in chunk j, tiles from kt on.
+// i >= j and, in chunk j, tiles from kt on.  The sequence repeats for each
+// of the `group` query heads qh0, qh0 + 1, ... that share the key tile.
 struct QTiles {
-    int P, C, j, causal, T, kt;
-    int i, qt;
-    __device__ __forceinline__ void init(int P_, int C_, int j_, int causal_, int T_, int kt_)
+    int P, C, j, causal, T, kt, group, qh0, per_head;
+    int i, qt, m, left;
+    __device__ __forceinline__ void init(int P_, int C_, int j_, int causal_, int T_, int kt_,
+                                         int group_, int qh0_)
     {
-        P = P_; C = C_; j = j_; causal = causal_; T = T_; kt = kt_;
+        P = P_; C = C_; j = j_; causal = causal_; T = T_; kt = kt_; group = group_; qh0 = qh0_;
+        per_head = causal ? (T - kt) + (P - 1 - j) * T : P * T;
+        m = 0;
+        left = per_head;
         i = j;
         qt = causal ? kt : 0;
     }
-    __device__ __forceinline__ int total() const
-    {
-        return causal ? (T - kt) + (P - 1 - j) * T : P * T;
-    }
+    __device__ __forceinline__ int total() const { return per_head * group; }
+    __device__ __forceinline__ int q_head() const { return qh0 + m; }
     __device__ __forceinline__ int q_start() const { return i * C + qt * kBQ; }
     __device__ __forceinline__ int chunk_end() const { return (i + 1) * C; }
     __device__ __forceinline__ void next()
     {
+        if (--left == 0) {               // this head is done: the next one in the group
+            ++m;
+            left = per_head;
+            i = j;
+            qt = causal ? kt : 0;
+            return;
+        }
         if (++qt < T) return;
         qt = 0;
         i = (i + 1 == P) ? 0 : i + 1;    // the chunk that meets j one ring step later
@@ -164,10 +178,13 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     const int lane = threadIdx.x & 31;
     const int wg = warp >> 2;
 
-    // ---- work item: (b*H + h, KV chunk j, key tile kt), heaviest first ----
+    // ---- work item: (b*H_kv + key/value head, KV chunk j, key tile kt),
+    // heaviest first ----
     const int T = p.tiles_per_chunk;
     const int items_per_head = p.P * T;
-    const int bh = blockIdx.x / items_per_head;
+    const int bkv = blockIdx.x / items_per_head;
+    const int H_kv = p.H / p.group;
+    const int qh0 = (bkv / H_kv) * p.H + (bkv % H_kv) * p.group;   // first query head of the group
     const int w = blockIdx.x % items_per_head;
     const int chunk_j = w / T;
     const int kt = w % T;
@@ -205,7 +222,7 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     const uint32_t tmem = *tmem_slot;
 
     QTiles qi;
-    qi.init(p.P, p.C, chunk_j, p.causal, T, kt);
+    qi.init(p.P, p.C, chunk_j, p.causal, T, kt, p.group, qh0);
     const int NT = qi.total();
 
     if (wg == 0) {
@@ -221,8 +238,8 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             }
             mbar_arrive_expect_tx(bar_kv, 2 * CF::kTileBytes);
             for (int x = 0; x < CF::kBoxes; ++x) {
-                tma_load_3d(sK + x * CF::kBoxBytes, &map_k, bar_kv, 64 * x, k0, bh);
-                tma_load_3d(sV + x * CF::kBoxBytes, &map_v, bar_kv, 64 * x, k0, bh);
+                tma_load_3d(sK + x * CF::kBoxBytes, &map_k, bar_kv, 64 * x, k0, bkv);
+                tma_load_3d(sV + x * CF::kBoxBytes, &map_v, bar_kv, 64 * x, k0, bkv);
             }
             int issued[CF::kStages];
             for (int s = 0; s < CF::kStages; ++s) issued[s] = -1;
@@ -234,17 +251,18 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 ok = mbar_wait(bar_qdo_empty(s), ph ^ 1u, wc);
                 if (!ok) break;
                 const int q0 = qi.q_start();
+                const int qh = qi.q_head();
                 mbar_arrive_expect_tx(bar_qdo_full(s), kStageTx);
                 for (int x = 0; x < CF::kBoxes; ++x) {
                     tma_load_3d(sQ + s * CF::kTileBytes + x * CF::kBoxBytes, &map_q,
-                                bar_qdo_full(s), 64 * x, q0, bh);
+                                bar_qdo_full(s), 64 * x, q0, qh);
                     tma_load_3d(sDO + s * CF::kTileBytes + x * CF::kBoxBytes, &map_do,
-                                bar_qdo_full(s), 64 * x, q0, bh);
+                                bar_qdo_full(s), 64 * x, q0, qh);
                 }
                 if constexpr (kRowTma) {
-                    tma_load_2d(sRow + s * 2 * CF::kRowBytes, &map_lse2, bar_qdo_full(s), q0, bh);
+                    tma_load_2d(sRow + s * 2 * CF::kRowBytes, &map_lse2, bar_qdo_full(s), q0, qh);
                     tma_load_2d(sRow + s * 2 * CF::kRowBytes + CF::kRowBytes, &map_dvec,
-                                bar_qdo_full(s), q0, bh);
+                                bar_qdo_full(s), q0, qh);
                 }
                 issued[s] = (int)ph;
             }
@@ -335,7 +353,7 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 for (int b = 0; b < D / 32; ++b) {
                     const uint32_t src = (b < D / 64 ? sQ : sDO) + s * CF::kTileBytes +
                                          (b % (D / 64)) * CF::kBoxBytes;
-                    tma_reduce_add_3d(&map_dq, src, 32 * b, q0, bh);
+                    tma_reduce_add_3d(&map_dq, src, 32 * b, q0, qi.q_head());
                 }
                 bulk_commit_group();
                 bulk_wait_read_all();
@@ -366,7 +384,7 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             const bool plain = key_ok && !diag && q_valid >= 32;
             const float* lse_s = reinterpret_cast<const float*>(smem + CF::kOffRow + s * 2 * CF::kRowBytes) + 32 * g;
             const float* d_s = lse_s + kBQ;
-            const size_t grow = (size_t)bh * p.S;
+            const size_t grow = (size_t)qi.q_head() * p.S;
             if constexpr (kRowTma) {
                 // the rows arrived with the Q / dO tile of this stage
                 ok = __all_sync(0xffffffffu,
@@ -505,7 +523,7 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             const uint32_t tAcc = tmem_addr(tmem, quarter * 32, (is_dk ? CF::kColDK : CF::kColDV) + col0);
             const float mul = is_dk ? p.scale : 1.f;
             __nv_bfloat16* out = (is_dk ? p.dk : p.dv) +
-                                 ((size_t)bh * p.S + (size_t)(key_ok ? kpos : 0)) * D + col0;
+                                 ((size_t)bkv * p.S + (size_t)(key_ok ? kpos : 0)) * D + col0;
 #pragma unroll
             for (int c4 = 0; c4 < D / 64; ++c4) {
                 uint32_t acc[32];
@@ -562,7 +580,7 @@ struct Launch {
     const void *q, *k, *v, *o, *dO;
     const float* lse;
     void *dq, *dk, *dv;
-    int B, H, S, d, P, causal;
+    int B, H, H_kv, S, d, P, causal;
     float scale;
     void* workspace;
     uint32_t* status;
@@ -603,10 +621,11 @@ inline int launch(const Launch& L, cudaError_t* err)
 
     CUtensorMap mq, mk, mv, mdo, mlse, mdv, mdq;
     const int BH = L.B * L.H;
+    const int BHkv = L.B * L.H_kv;
     const int C = L.S / L.P;
     const bool row_tma = (C % 4) == 0;
-    if (L.encode(&mq, L.q, BH, L.S, L.d, kBQ) || L.encode(&mk, L.k, BH, L.S, L.d, kBK) ||
-        L.encode(&mv, L.v, BH, L.S, L.d, kBK) || L.encode(&mdo, L.dO, BH, L.S, L.d, kBQ)) {
+    if (L.encode(&mq, L.q, BH, L.S, L.d, kBQ) || L.encode(&mk, L.k, BHkv, L.S, L.d, kBK) ||
+        L.encode(&mv, L.v, BHkv, L.S, L.d, kBK) || L.encode(&mdo, L.dO, BH, L.S, L.d, kBQ)) {
         *err = cudaErrorInvalidValue;
         return -3;
     }
@@ -631,11 +650,13 @@ inline int launch(const Launch& L, cudaError_t* err)
     prm.C = C;
     prm.causal = L.causal;
     prm.tiles_per_chunk = (prm.C + kBK - 1) / kBK;
+    prm.H = L.H;
+    prm.group = L.H / L.H_kv;
     prm.scale = L.scale;
     prm.scale_log2 = (float)((double)L.scale * 1.4426950408889634);
     prm.status = L.status;
     prm.wait_limit_ns = L.wait_limit_ns;
-    const long long grid = (long long)BH * L.P * prm.tiles_per_chunk;
+    const long long grid = (long long)BHkv * L.P * prm.tiles_per_chunk;
     {
         prof::Scope ps(prof::kBwdMain, L.stream);
         const dim3 g((unsigned)grid), b(kThreads);

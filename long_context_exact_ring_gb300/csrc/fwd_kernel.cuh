@@ -72,6 +72,7 @@ struct FwdParams {
     __nv_bfloat16* o;       // [B, H, S, D]
     float* lse;             // [B, H, S]
     int S, P, C;            // sequence, chunks, chunk length
+    int H, group;           // query heads; query heads per key/value head
     int causal;
     int pairs_per_chunk;    // ceil(C / 256)
     float scale_log2;       // scale * log2(e)
@@ -148,6 +149,9 @@ ring_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     const int chunk_i = g / p.pairs_per_chunk;
     const int q0 = chunk_i * p.C + (g % p.pairs_per_chunk) * kRowsPerCta;
     const int q_end = min(q0 + kRowsPerCta, (chunk_i + 1) * p.C);   // rows stored
+    // key/value head of this query head (grouped-query attention: query
+    // head h reads key/value head h / group)
+    const int bkv = (bh / p.H) * (p.H / p.group) + (bh % p.H) / p.group;
 
     WaitCtl wc{abort_flag, p.status, p.wait_limit_ns};
 
@@ -204,14 +208,14 @@ ring_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 mbar_arrive_expect_tx(bar_k_full(s), CF::kTileBytes);
                 for (int x = 0; x < CF::kBoxes; ++x)
                     tma_load_3d(sK + s * CF::kTileBytes + x * CF::kBoxBytes, &map_k,
-                                bar_k_full(s), 64 * x, key0, bh);
+                                bar_k_full(s), 64 * x, key0, bkv);
                 issued_k[s] = (int)ph;
                 ok = mbar_wait(bar_v_empty(s), ph ^ 1u, wc);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar_v_full(s), CF::kTileBytes);
                 for (int x = 0; x < CF::kBoxes; ++x)
                     tma_load_3d(sV + s * CF::kTileBytes + x * CF::kBoxBytes, &map_v,
-                                bar_v_full(s), 64 * x, key0, bh);
+                                bar_v_full(s), 64 * x, key0, bkv);
                 issued_v[s] = (int)ph;
             }
             if (!ok) {

@@ -240,11 +240,16 @@ int ring_attn_schedule(int P, int causal, int i, int* out_j, int* out_kind, int 
     return n;
 }
 
-int ring_attn_fwd(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, ra_bf16* o, float* lse,
-                  int B, int H, int S, int d, int P, int causal, float scale, void* stream)
+}  // extern "C"
+
+namespace {
+
+int fwd_impl(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, ra_bf16* o, float* lse, int B,
+             int H, int H_kv, int S, int d, int P, int causal, float scale, void* stream)
 {
     int rc = check_shape(B, H, S, d, P, causal, scale);
     if (rc != RA_OK) return rc;
+    if (H_kv < 1 ? H != 0 : (H % H_kv) != 0) return RA_ERR_INVALID_ARG;
     if ((long long)B * H * S == 0) return RA_OK;
     if (!q || !k || !v || !o || !lse) return RA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
@@ -261,8 +266,8 @@ int ring_attn_fwd(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, ra_bf16*
     CUtensorMap mq, mk, mv;
     const int BH = B * H;
     if ((rc = make_map(&mq, q, BH, S, d, ra::fwd::kBM)) != RA_OK) return rc;
-    if ((rc = make_map(&mk, k, BH, S, d, ra::fwd::kBN)) != RA_OK) return rc;
-    if ((rc = make_map(&mv, v, BH, S, d, ra::fwd::kBN)) != RA_OK) return rc;
+    if ((rc = make_map(&mk, k, B * H_kv, S, d, ra::fwd::kBN)) != RA_OK) return rc;
+    if ((rc = make_map(&mv, v, B * H_kv, S, d, ra::fwd::kBN)) != RA_OK) return rc;
 
     ra::fwd::FwdParams prm;
     prm.o = reinterpret_cast<__nv_bfloat16*>(o);
@@ -272,6 +277,8 @@ int ring_attn_fwd(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, ra_bf16*
     prm.C = C;
     prm.causal = causal;
     prm.pairs_per_chunk = (int)pairs;
+    prm.H = H;
+    prm.group = H / H_kv;
     prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
     prm.status = st->status;
     prm.wait_limit_ns = g_wait_limit_ns.load();
@@ -289,6 +296,28 @@ int ring_attn_fwd(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, ra_bf16*
     return RA_OK;
 }
 
+int bwd_impl(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, const ra_bf16* o,
+             const float* lse, const ra_bf16* dO, ra_bf16* dq, ra_bf16* dk, ra_bf16* dv, int B,
+             int H, int H_kv, int S, int d, int P, int causal, float scale, void* workspace,
+             size_t workspace_bytes, void* stream);
+
+}  // namespace
+
+extern "C" {
+
+int ring_attn_fwd(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, ra_bf16* o, float* lse,
+                  int B, int H, int S, int d, int P, int causal, float scale, void* stream)
+{
+    return fwd_impl(q, k, v, o, lse, B, H, H, S, d, P, causal, scale, stream);
+}
+
+int ring_attn_fwd_gqa(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, ra_bf16* o, float* lse,
+                      int B, int H, int H_kv, int S, int d, int P, int causal, float scale,
+                      void* stream)
+{
+    return fwd_impl(q, k, v, o, lse, B, H, H_kv, S, d, P, causal, scale, stream);
+}
+
 size_t ring_attn_bwd_workspace_size(int B, int H, int S, int d)
 {
     if (B <= 0 || H <= 0 || S <= 0 || d <= 0) return 0;
@@ -300,8 +329,31 @@ int ring_attn_bwd(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, const ra
                   int B, int H, int S, int d, int P, int causal, float scale, void* workspace,
                   size_t workspace_bytes, void* stream)
 {
+    return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, H, S, d, P, causal, scale, workspace,
+                    workspace_bytes, stream);
+}
+
+int ring_attn_bwd_gqa(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, const ra_bf16* o,
+                      const float* lse, const ra_bf16* dO, ra_bf16* dq, ra_bf16* dk, ra_bf16* dv,
+                      int B, int H, int H_kv, int S, int d, int P, int causal, float scale,
+                      void* workspace, size_t workspace_bytes, void* stream)
+{
+    return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, H_kv, S, d, P, causal, scale, workspace,
+                    workspace_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+int bwd_impl(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, const ra_bf16* o,
+             const float* lse, const ra_bf16* dO, ra_bf16* dq, ra_bf16* dk, ra_bf16* dv, int B,
+             int H, int H_kv, int S, int d, int P, int causal, float scale, void* workspace,
+             size_t workspace_bytes, void* stream)
+{
     int rc = check_shape(B, H, S, d, P, causal, scale);
     if (rc != RA_OK) return rc;
+    if (H_kv < 1 ? H != 0 : (H % H_kv) != 0) return RA_ERR_INVALID_ARG;
     if ((long long)B * H * S == 0) return RA_OK;
     if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)
         return RA_ERR_INVALID_ARG;
@@ -316,7 +368,7 @@ int ring_attn_bwd(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, const ra
     ra::bwd::Launch L;
     L.q = q; L.k = k; L.v = v; L.o = o; L.lse = lse; L.dO = dO;
     L.dq = dq; L.dk = dk; L.dv = dv;
-    L.B = B; L.H = H; L.S = S; L.d = d; L.P = P; L.causal = causal; L.scale = scale;
+    L.B = B; L.H = H; L.H_kv = H_kv; L.S = S; L.d = d; L.P = P; L.causal = causal; L.scale = scale;
     L.workspace = workspace;
     L.status = st->status;
     L.num_sms = st->num_sms;
@@ -336,6 +388,10 @@ int ring_attn_bwd(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, const ra
     if (rc == RA_ERR_CUDA) return fail_cuda(e, "ring_bwd launch");
     return rc;
 }
+
+}  // namespace
+
+extern "C" {
 
 int ring_attn_bwd_noalloc(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, const ra_bf16* o,
                           const float* lse, const ra_bf16* dO, ra_bf16* dq, ra_bf16* dk, ra_bf16* dv,

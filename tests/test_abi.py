@@ -115,6 +115,20 @@ def test_bwd_validates_before_any_launch(lib):
     assert call(ptr=FAKE + 4) == -1
 
 
+def test_gqa_validates_before_any_launch(lib):
+    def fwd(H=4, Hkv=2, ptr=FAKE, S=256, P=4):
+        return lib.ring_attn_fwd_gqa(ptr, ptr, ptr, ptr, ptr, 1, H, Hkv, S, 128, P, 1, 0.1, None)
+    assert fwd(H=4, Hkv=3) == -1                       # H not a multiple of H_kv
+    assert fwd(Hkv=0) == -1
+    assert fwd(Hkv=-2) == -1
+    assert fwd(S=250) == -1
+    assert fwd(ptr=FAKE + 8) == -1
+    assert fwd(H=0, Hkv=0, ptr=0) == 0                 # empty
+    ws = lib.ring_attn_bwd_workspace_size(1, 4, 256, 128)
+    assert lib.ring_attn_bwd_gqa(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 3, 256,
+                                 128, 4, 1, 0.1, FAKE, ws, None) == -1
+
+
 def test_merge_validates_before_any_launch(lib):
     def call(a=FAKE, b=FAKE * 2, out=FAKE * 3, la=FAKE * 4, lb=FAKE * 5, lout=FAKE * 6, d=64):
         return lib.attn_merge_partials(a, la, b, lb, out, lout, 1, 2, 8, d, None)

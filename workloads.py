@@ -15,6 +15,8 @@ Recipe (the pages print no generator, so this is the plain reading):
 The oracle receives the bf16 values widened to float64, so both sides see
 identical inputs.
 
+Grouped-query workloads draw k and v with H_kv heads.
+
 Shapes follow the pages' worked example ("Context Parallelism" guide,
 section 2, "Worked Example": 32 heads, d_k = 128, S = 128K, CP = 4) and the
 smaller and peaked variants around it.
@@ -40,6 +42,7 @@ class Workload:
     peaked_keys: bool = False   # key rows c % 64 == 0 scaled x8
     v_uniform: bool = False     # V ~ U(-1, 1) instead of N(0, 1)
     backward: bool = False      # also draw dO
+    H_kv: int = 0               # key/value heads (grouped-query); 0 means H
     note: str = field(default="", compare=False)
 
     @property
@@ -62,12 +65,18 @@ FWD_PEAKED_64K = Workload("fwd_peaked_b2_h16_s65536_d128_p8", 2, 16, 65536, 128,
                           peaked_keys=True, v_uniform=True)
 FWDBWD_CAUSAL_128K = Workload("fwdbwd_causal_h32_s131072_d128_p4", 1, 32, 131072, 128, 4, True, 4,
                               backward=True)
+# Grouped-query variant of the 128K shape: 32 query heads over 8 key/value
+# heads (the pages' example of a model with 8 KV heads, "Ring Attention vs.
+# DeepSpeed Ulysses").
+FWDBWD_GQA_128K = Workload("fwdbwd_gqa_h32_kv8_s131072_d128_p4", 1, 32, 131072, 128, 4, True, 5,
+                           backward=True, H_kv=8)
 
-ALL = [TINY_F32, FWD_CAUSAL_32K, FWD_CAUSAL_128K, FWD_PEAKED_64K, FWDBWD_CAUSAL_128K]
+ALL = [TINY_F32, FWD_CAUSAL_32K, FWD_CAUSAL_128K, FWD_PEAKED_64K, FWDBWD_CAUSAL_128K,
+       FWDBWD_GQA_128K]
 
 
 def make(w: Workload, *, B=None, H=None, S=None, d=None, P=None, causal=None,
-         seed=None, backward=None, device="cpu", keep_fp32=True):
+         seed=None, backward=None, device="cpu", keep_fp32=True, H_kv=None):
     """Draw the inputs of workload ``w`` (optionally with overridden sizes).
 
     Returns a dict with fp32 tensors ``q32, k32, v32`` (and ``do32``) exactly
@@ -77,6 +86,7 @@ def make(w: Workload, *, B=None, H=None, S=None, d=None, P=None, causal=None,
     stream from the CPU one; used where only throughput is measured) and
     ``keep_fp32=False`` drops the fp32 copies.
     """
+    h_given = H
     B = w.B if B is None else B
     H = w.H if H is None else H
     S = w.S if S is None else S
@@ -85,15 +95,20 @@ def make(w: Workload, *, B=None, H=None, S=None, d=None, P=None, causal=None,
     causal = w.causal if causal is None else causal
     seed = w.seed if seed is None else seed
     backward = w.backward if backward is None else backward
+    if H_kv is None:
+        # the workload's own grouping, unless the query heads were overridden
+        H_kv = (w.H_kv or w.H) if h_given is None else H
     g = torch.Generator(device).manual_seed(seed)
     shape = (B, H, S, d)
-    out = dict(B=B, H=H, S=S, d=d, P=P, causal=causal, scale=1.0 / math.sqrt(d))
+    kv_shape = (B, H_kv, S, d)
+    out = dict(B=B, H=H, H_kv=H_kv, S=S, d=d, P=P, causal=causal, scale=1.0 / math.sqrt(d))
 
-    def draw(name, uniform=False, peaked=False):
+    def draw(name, uniform=False, peaked=False, kv=False):
+        shp = kv_shape if kv else shape
         if uniform:
-            x = torch.rand(shape, generator=g, dtype=torch.float32, device=device) * 2 - 1
+            x = torch.rand(shp, generator=g, dtype=torch.float32, device=device) * 2 - 1
         else:
-            x = torch.randn(shape, generator=g, dtype=torch.float32, device=device)
+            x = torch.randn(shp, generator=g, dtype=torch.float32, device=device)
         if peaked:
             x[:, :, 0::64, :] *= 8.0
         out[name] = x.to(torch.bfloat16)
@@ -101,8 +116,8 @@ def make(w: Workload, *, B=None, H=None, S=None, d=None, P=None, causal=None,
             out[name + "32"] = x
 
     draw("q")
-    draw("k", peaked=w.peaked_keys)
-    draw("v", uniform=w.v_uniform)
+    draw("k", peaked=w.peaked_keys, kv=True)
+    draw("v", uniform=w.v_uniform, kv=True)
     if backward:
         draw("do")
     return out
