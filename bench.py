@@ -72,6 +72,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-ring-emulation", action="store_true",
+                    help="skip the emulated-ring forward (P logical ranks, copy-stream rotation)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle sample")
     ap.add_argument("--seq", type=int, default=None,
@@ -396,6 +398,40 @@ def main():
                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in.values()),
                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out)}
 
+    # ---- emulated ring: the pages' protocol with P logical ranks ----------
+    emu = None
+    if not args.no_ring_emulation and inp.get("H_kv", H) == H:
+        ws_e = torch.empty(ra.emulated_workspace_size(B, H, S, d), dtype=torch.uint8, device="cuda")
+        o_e = torch.empty_like(q)
+        lse_e = torch.empty_like(lse)
+
+        def timed(fn, reps=3):
+            fn()
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / reps
+
+        fused = timed(lambda: ra.ring_attn_fwd(q, k, v, P, causal, sc, o=o, lse=lse, stream=stream))
+        over = timed(lambda: ra.ring_attn_fwd_emulated(q, k, v, P, causal, sc, overlap=True, o=o_e,
+                                                       lse=lse_e, workspace=ws_e, stream=stream))
+        serial = timed(lambda: ra.ring_attn_fwd_emulated(q, k, v, P, causal, sc, overlap=False, o=o_e,
+                                                         lse=lse_e, workspace=ws_e, stream=stream))
+        if ra.check_status() != ra.RA_OK:
+            raise RuntimeError("a kernel reported a bounded-wait timeout in the ring emulation")
+        step_bytes = 2 * S * d * 2 * B * H      # every rank's K and V chunk, all heads
+        del ws_e
+        emu = {"pass": "fwd", "P": P, "fused_fwd_ms": fused, "emulated_overlapped_ms": over,
+               "emulated_serialized_ms": serial,
+               "rotation_bytes_per_step": step_bytes, "rotations": P - 1,
+               "rotation_cost_serialized_ms": serial - over,
+               "emulated_overlapped_tflops": f_fwd / (over / 1e3) / 1e12}
+
     # ---- CPU oracle baseline (rank 0, one GPU only) ------------------------
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -417,6 +453,7 @@ def main():
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "ring_emulation": emu,
             "gpu_launches": launches,
             "kernels": {n: {"launches": c, "ms": m} for n, (c, m) in prof.items() if c},
             "clocks": clk,

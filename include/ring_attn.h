@@ -171,6 +171,38 @@ int ring_attn_bwd_noalloc(const ra_bf16 *q, const ra_bf16 *k, const ra_bf16 *v, 
                           void *stream);
 
 /*
+ * Bytes of device workspace ring_attn_fwd_emulated needs: two receive
+ * buffers of K and V for the P logical ranks (4 x B*H*S*d bf16), the running
+ * and the per-step fp32 O (2 x B*H*S*d fp32) and the per-step LSE, each
+ * 256-byte aligned.  0 for an empty or invalid shape.
+ */
+size_t ring_attn_fwd_emulated_workspace_size(int B, int H, int S, int d);
+
+/*
+ * The pages' ring protocol emulated literally with P logical ranks on one
+ * GPU ("Training Long-Context Models Without OOM: Ring Attention", "Ring
+ * Attention Demystified", steps 2-5; "Context Parallelism" guide, section 2,
+ * "How It Works" and "Communication").  Rank i owns query chunk Q_i and a
+ * private K/V receive buffer that starts with K_i, V_i.  At ring step t each
+ * rank computes the partial attention of Q_i against the chunk it holds
+ * (KV chunk (i - t) mod P; nothing for j > i when causal) and folds it into
+ * its running (O, LSE) with attn_merge_partials.  Meanwhile every rank sends
+ * its chunk to rank (i + 1) % P: device-to-device copies into the other
+ * receive buffer on a separate copy stream ("the interconnect"), ordered by
+ * events, so the rotation overlaps the step's compute (overlap = 1).  With
+ * overlap = 0 the copies run on `stream` between the steps instead, which
+ * measures the rotation's cost.  The result equals ring_attn_fwd (O bf16,
+ * LSE fp32); P is merged in fp32 and rounded to bf16 once at the end.
+ * Arguments as ring_attn_fwd, plus the caller-owned workspace (256-byte
+ * aligned, ring_attn_fwd_emulated_workspace_size bytes).  The copy stream
+ * and its events are created on the first call on a device and kept.
+ * Concurrent calls on one device share them and must be ordered.
+ */
+int ring_attn_fwd_emulated(const ra_bf16 *q, const ra_bf16 *k, const ra_bf16 *v, ra_bf16 *o,
+                           float *lse, int B, int H, int S, int d, int P, int causal, float scale,
+                           void *workspace, size_t workspace_bytes, int overlap, void *stream);
+
+/*
  * Log-sum-exp merge of two partial attention results of the same query rows
  * (the merge each ring step performs; "Context Parallelism" guide, section
  * 2: partial results are merged with the online-softmax statistics):

@@ -29,6 +29,8 @@ from ._binding import (  # noqa: F401
     ring_attn_bwd_noalloc,
     NOALLOC_SCRATCH_BYTES,
     ring_attn_fwd,
+    ring_attn_fwd_emulated,
+    emulated_workspace_size,
     ring_schedule,
     set_wait_limit_ns,
     status_string,

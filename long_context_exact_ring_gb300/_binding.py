@@ -29,6 +29,8 @@ EXPORTED = (
     "ring_attn_fwd_gqa",
     "ring_attn_bwd_gqa",
     "ring_attn_bwd_workspace_size",
+    "ring_attn_fwd_emulated",
+    "ring_attn_fwd_emulated_workspace_size",
     "ring_attn_bwd",
     "ring_attn_bwd_noalloc",
     "attn_merge_partials",
@@ -74,6 +76,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.ring_attn_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i,
                                           f, vp, sz, vp]
         lib.ring_attn_bwd_gqa.restype = i
+        lib.ring_attn_fwd_emulated.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, sz, i, vp]
+        lib.ring_attn_fwd_emulated.restype = i
+        lib.ring_attn_fwd_emulated_workspace_size.argtypes = [i, i, i, i]
+        lib.ring_attn_fwd_emulated_workspace_size.restype = sz
         lib.ring_attn_bwd_workspace_size.argtypes = [i, i, i, i]
         lib.ring_attn_bwd_workspace_size.restype = sz
         lib.ring_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f,
@@ -183,6 +189,40 @@ def ring_attn_fwd(q, k, v, P: int, causal: bool, scale: float | None = None, *,
                                    lse.data_ptr(), B, H, H_kv, S, d, int(P), int(bool(causal)),
                                    float(scale), _stream(stream))
     _check(rc, "ring_attn_fwd")
+    return o, lse
+
+
+def emulated_workspace_size(B: int, H: int, S: int, d: int) -> int:
+    return int(load_library().ring_attn_fwd_emulated_workspace_size(B, H, S, d))
+
+
+def ring_attn_fwd_emulated(q, k, v, P: int, causal: bool, scale: float | None = None, *,
+                           overlap: bool = True, o=None, lse=None, workspace=None, stream=None):
+    """The ring protocol with P logical ranks on one GPU: per-step partials
+    merged with the LSE merge while a copy stream rotates each rank's K/V
+    chunk to the next rank (overlap=False puts the copies between steps)."""
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, S, d]")
+    B, H, S, d = q.shape
+    _need(k, "k", torch.bfloat16, q.shape)
+    _need(v, "v", torch.bfloat16, q.shape)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(o, "o", torch.bfloat16, q.shape)
+    _need(lse, "lse", torch.float32, (B, H, S))
+    need = emulated_workspace_size(B, H, S, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _need(workspace, "workspace", torch.uint8)
+    rc = load_library().ring_attn_fwd_emulated(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                               o.data_ptr(), lse.data_ptr(), B, H, S, d, int(P),
+                                               int(bool(causal)), float(scale), workspace.data_ptr(),
+                                               workspace.numel(), int(bool(overlap)),
+                                               _stream(stream))
+    _check(rc, "ring_attn_fwd_emulated")
     return o, lse
 
 

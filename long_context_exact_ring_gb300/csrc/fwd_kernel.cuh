@@ -73,6 +73,12 @@ struct FwdParams {
     float* lse;             // [B, H, S]
     int S, P, C;            // sequence, chunks, chunk length
     int H, group;           // query heads; query heads per key/value head
+    // Emulated ring (one step at a time): step >= 0 restricts the CTA to KV
+    // chunk j = (i - step) mod P, read from rank i's receive buffer -- a
+    // [P * B * H, C, D] tensor whose head index is i * BH + bh -- and writes
+    // the normalized partial O in fp32 to o32.  step = -1 is the fused ring.
+    int step, BH;
+    float* o32;
     int causal;
     int pairs_per_chunk;    // ceil(C / 256)
     float scale_log2;       // scale * log2(e)
@@ -93,6 +99,23 @@ struct RingTiles {
         tiles_per_chunk = (C + kBN - 1) / kBN;
         tiles_local = causal ? (q_last_excl - i * C + kBN - 1) / kBN : tiles_per_chunk;
         t = 0; j = i; kt = 0; kt_count = tiles_local;
+    }
+    // One ring step only: chunk j = (i - t) mod P; nothing when causal and
+    // j > i.
+    __device__ __forceinline__ void init_step(int P_, int C_, int i_, int t_, int causal_, int q_last_excl)
+    {
+        P = P_; C = C_; i = i_; causal = causal_;
+        tiles_per_chunk = (C + kBN - 1) / kBN;
+        t = t_;
+        j = ((i - t) % P + P) % P;
+        if (causal && j > i)
+            kt_count = 0;
+        else if (causal && j == i)
+            kt_count = (q_last_excl - i * C + kBN - 1) / kBN;
+        else
+            kt_count = tiles_per_chunk;
+        tiles_local = kt_count;
+        kt = 0;
     }
     __device__ __forceinline__ int total() const
     {
@@ -181,11 +204,35 @@ ring_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    const bool step_mode = p.step >= 0;
     RingTiles rt;
-    rt.init(p.P, p.C, chunk_i, p.causal, q_end);
-    const int NT = rt.total();
+    int NT;
+    if (step_mode) {
+        rt.init_step(p.P, p.C, chunk_i, p.step, p.causal, q_end);
+        NT = rt.kt_count;
+    } else {
+        rt.init(p.P, p.C, chunk_i, p.causal, q_end);
+        NT = rt.total();
+    }
+    // K/V source: the key/value head of the fused ring, or this rank's
+    // receive buffer (rows relative to the chunk start) in step mode.
+    const int kv_head = step_mode ? chunk_i * p.BH + bh : bkv;
+    const int kv_row0 = step_mode ? rt.j * p.C : 0;
 
-    if (warp == 0) {
+    if (NT == 0) {
+        // Nothing to attend to in this ring step (causal, chunk above the
+        // diagonal): the partial is the merge identity, O = 0, LSE = -inf.
+        if (warp >= 2) {
+            const int u = (warp - 2) >> 2;
+            const int row = q0 + kBM * u + (warp & 3) * 32 + lane;
+            if (row < q_end && p.o32) {
+                float4* dst = reinterpret_cast<float4*>(p.o32 + ((size_t)bh * p.S + row) * D);
+#pragma unroll
+                for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                p.lse[(size_t)bh * p.S + row] = -INFINITY;
+            }
+        }
+    } else if (warp == 0) {
         // ------------------------------------------------------------ TMA
         if (lane == 0) {
             tma_prefetch_desc(&map_q);
@@ -208,14 +255,14 @@ ring_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 mbar_arrive_expect_tx(bar_k_full(s), CF::kTileBytes);
                 for (int x = 0; x < CF::kBoxes; ++x)
                     tma_load_3d(sK + s * CF::kTileBytes + x * CF::kBoxBytes, &map_k,
-                                bar_k_full(s), 64 * x, key0, bkv);
+                                bar_k_full(s), 64 * x, key0 - kv_row0, kv_head);
                 issued_k[s] = (int)ph;
                 ok = mbar_wait(bar_v_empty(s), ph ^ 1u, wc);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar_v_full(s), CF::kTileBytes);
                 for (int x = 0; x < CF::kBoxes; ++x)
                     tma_load_3d(sV + s * CF::kTileBytes + x * CF::kBoxBytes, &map_v,
-                                bar_v_full(s), 64 * x, key0, bkv);
+                                bar_v_full(s), 64 * x, key0 - kv_row0, kv_head);
                 issued_v[s] = (int)ph;
             }
             if (!ok) {
@@ -327,7 +374,7 @@ ring_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&s[96]));
             const int key0 = rt.key_start();
             const int kend = rt.chunk_end();
-            const bool local = rt.j == chunk_i;
+            const bool local = rt.j == chunk_i;   // the query chunk's own KV chunk
             // Masking is needed on a tile that runs past its chunk's end or,
             // causal, on the local chunk's tiles that reach above row q0+128u.
             const bool need_mask = (key0 + kBN > kend) ||
@@ -383,22 +430,35 @@ ring_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             tc_fence_after();
             const bool store = row < q_end;
             const float inv_l = 1.f / l;
-            __nv_bfloat16* orow = p.o + ((size_t)bh * p.S + (size_t)(store ? row : 0)) * D;
+            const size_t orow_off = ((size_t)bh * p.S + (size_t)(store ? row : 0)) * D;
 #pragma unroll
             for (int c4 = 0; c4 < D / 32; ++c4) {
                 uint32_t o[32];
                 tmem_ld32(tO + 32u * c4, o);
                 tmem_ld_wait(o);
-                uint32_t pk[16];
+                if (p.o32) {
+                    // partial of one ring step, fp32 for the merge
+                    if (store) {
+                        float4* dst = reinterpret_cast<float4*>(p.o32 + orow_off + 32 * c4);
 #pragma unroll
-                for (int c = 0; c < 16; ++c)
-                    pk[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l,
-                                        __uint_as_float(o[2 * c + 1]) * inv_l);
-                if (store) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c4);
+                        for (int v4 = 0; v4 < 8; ++v4)
+                            dst[v4] = make_float4(__uint_as_float(o[4 * v4]) * inv_l,
+                                                  __uint_as_float(o[4 * v4 + 1]) * inv_l,
+                                                  __uint_as_float(o[4 * v4 + 2]) * inv_l,
+                                                  __uint_as_float(o[4 * v4 + 3]) * inv_l);
+                    }
+                } else {
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4)
-                        dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                    for (int c = 0; c < 16; ++c)
+                        pk[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l,
+                                            __uint_as_float(o[2 * c + 1]) * inv_l);
+                    if (store) {
+                        uint4* dst = reinterpret_cast<uint4*>(p.o + orow_off + 32 * c4);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                    }
                 }
             }
             if (store) p.lse[(size_t)bh * p.S + row] = (m_used + log2f(l)) * 0.69314718055994531f;

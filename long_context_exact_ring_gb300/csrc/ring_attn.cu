@@ -279,6 +279,9 @@ int fwd_impl(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, ra_bf16* o, f
     prm.pairs_per_chunk = (int)pairs;
     prm.H = H;
     prm.group = H / H_kv;
+    prm.step = -1;
+    prm.BH = BH;
+    prm.o32 = nullptr;
     prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
     prm.status = st->status;
     prm.wait_limit_ns = g_wait_limit_ns.load();
@@ -301,6 +304,61 @@ int bwd_impl(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, const ra_bf16
              int H, int H_kv, int S, int d, int P, int causal, float scale, void* workspace,
              size_t workspace_bytes, void* stream);
 
+// ---------------------------------------------------------------------------
+// Emulated ring: P logical ranks on one GPU
+// ---------------------------------------------------------------------------
+// Per device: a non-blocking copy stream (the "interconnect") and the events
+// that order it against the compute stream; created on first use, kept.
+struct RingRuntime {
+    bool ready = false;
+    cudaStream_t copy = nullptr;
+    cudaEvent_t init_done = nullptr, copied[2] = {}, consumed[2] = {};
+};
+RingRuntime g_ring[kMaxDevices];
+std::mutex g_ring_mu;
+
+int ring_runtime(RingRuntime** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return RA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_ring_mu);
+    RingRuntime& r = g_ring[dev];
+    if (!r.ready) {
+        e = cudaStreamCreateWithFlags(&r.copy, cudaStreamNonBlocking);
+        cudaEvent_t* evs[5] = {&r.init_done, &r.copied[0], &r.copied[1], &r.consumed[0], &r.consumed[1]};
+        for (int x = 0; x < 5 && e == cudaSuccess; ++x)
+            e = cudaEventCreateWithFlags(evs[x], cudaEventDisableTiming);
+        if (e != cudaSuccess) return fail_cuda(e, "ring runtime set-up");
+        r.ready = true;
+    }
+    *out = &r;
+    return RA_OK;
+}
+
+struct EmuLayout {
+    size_t kv_buf;      // one K (or V) receive buffer set: P ranks x B*H heads x C rows x d
+    size_t off_k[2], off_v[2], off_o, off_part, off_lse, total;
+};
+
+EmuLayout emu_layout(int B, int H, int S, int d)
+{
+    EmuLayout L;
+    const size_t rows = (size_t)B * H * S;
+    L.kv_buf = ra::bwd::align256(rows * d * 2);
+    size_t off = 0;
+    for (int b = 0; b < 2; ++b) {
+        L.off_k[b] = off; off += L.kv_buf;
+        L.off_v[b] = off; off += L.kv_buf;
+    }
+    L.off_o = off; off += ra::bwd::align256(rows * d * 4);
+    L.off_part = off; off += ra::bwd::align256(rows * d * 4);
+    L.off_lse = off; off += ra::bwd::align256(rows * 4);
+    L.total = off;
+    return L;
+}
+
 }  // namespace
 
 extern "C" {
@@ -316,6 +374,134 @@ int ring_attn_fwd_gqa(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, ra_b
                       void* stream)
 {
     return fwd_impl(q, k, v, o, lse, B, H, H_kv, S, d, P, causal, scale, stream);
+}
+
+size_t ring_attn_fwd_emulated_workspace_size(int B, int H, int S, int d)
+{
+    if (B <= 0 || H <= 0 || S <= 0 || d <= 0) return 0;
+    return emu_layout(B, H, S, d).total;
+}
+
+int ring_attn_fwd_emulated(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, ra_bf16* o,
+                           float* lse, int B, int H, int S, int d, int P, int causal, float scale,
+                           void* workspace, size_t workspace_bytes, int overlap, void* stream)
+{
+    int rc = check_shape(B, H, S, d, P, causal, scale);
+    if (rc != RA_OK) return rc;
+    if (overlap != 0 && overlap != 1) return RA_ERR_INVALID_ARG;
+    if ((long long)B * H * S == 0) return RA_OK;
+    if (!q || !k || !v || !o || !lse || !workspace) return RA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return RA_ERR_INVALID_ARG;
+    const EmuLayout lay = emu_layout(B, H, S, d);
+    if (workspace_bytes < lay.total) return RA_ERR_INVALID_ARG;
+    const int C = S / P;
+    const long long pairs = (C + ra::fwd::kRowsPerCta - 1) / ra::fwd::kRowsPerCta;
+    const long long grid = (long long)B * H * P * pairs;
+    if (grid > 0x7fffffffll) return RA_ERR_UNSUPPORTED;
+    DeviceState* st = nullptr;
+    if ((rc = device_state(&st)) != RA_OK) return rc;
+    RingRuntime* rr = nullptr;
+    if ((rc = ring_runtime(&rr)) != RA_OK) return rc;
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    ra_bf16* kbuf[2] = {reinterpret_cast<ra_bf16*>(ws + lay.off_k[0]), reinterpret_cast<ra_bf16*>(ws + lay.off_k[1])};
+    ra_bf16* vbuf[2] = {reinterpret_cast<ra_bf16*>(ws + lay.off_v[0]), reinterpret_cast<ra_bf16*>(ws + lay.off_v[1])};
+    float* o_run = reinterpret_cast<float*>(ws + lay.off_o);
+    float* o_part = reinterpret_cast<float*>(ws + lay.off_part);
+    float* lse_part = reinterpret_cast<float*>(ws + lay.off_lse);
+    const int BH = B * H;
+    const size_t chunk_bytes = (size_t)C * d * 2;          // one head's chunk
+    const size_t rank_bytes = (size_t)BH * chunk_bytes;    // one rank's K (or V)
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaStream_t xs = overlap ? rr->copy : cs;             // the interconnect
+    cudaError_t e = cudaSuccess;
+
+    // Step 0 set-up: every rank holds its own chunk (K_i, V_i) in buffer 0.
+    for (int i = 0; i < P && e == cudaSuccess; ++i) {
+        e = cudaMemcpy2DAsync(reinterpret_cast<uint8_t*>(kbuf[0]) + (size_t)i * rank_bytes, chunk_bytes,
+                              reinterpret_cast<const uint8_t*>(k) + (size_t)i * chunk_bytes,
+                              (size_t)S * d * 2, chunk_bytes, BH, cudaMemcpyDeviceToDevice, cs);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(reinterpret_cast<uint8_t*>(vbuf[0]) + (size_t)i * rank_bytes, chunk_bytes,
+                                  reinterpret_cast<const uint8_t*>(v) + (size_t)i * chunk_bytes,
+                                  (size_t)S * d * 2, chunk_bytes, BH, cudaMemcpyDeviceToDevice, cs);
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(rr->init_done, cs);
+    if (e != cudaSuccess) return fail_cuda(e, "ring set-up copies");
+
+    CUtensorMap mq;
+    if ((rc = make_map(&mq, q, BH, S, d, ra::fwd::kBM)) != RA_OK) return rc;
+    for (int t = 0; t < P; ++t) {
+        const int cur = t & 1, nxt = cur ^ 1;
+        // Rotation for step t + 1 on the interconnect: rank i sends the
+        // chunk it holds to rank (i + 1) % P, into the other buffer -- once
+        // step t - 1 has finished reading that buffer.
+        if (t + 1 < P) {
+            if (t == 0) e = cudaStreamWaitEvent(xs, rr->init_done, 0);
+            else e = cudaStreamWaitEvent(xs, rr->consumed[nxt], 0);
+            for (int i = 0; i < P && e == cudaSuccess; ++i) {
+                const size_t src = (size_t)i * rank_bytes, dst = (size_t)((i + 1) % P) * rank_bytes;
+                e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(kbuf[nxt]) + dst,
+                                    reinterpret_cast<uint8_t*>(kbuf[cur]) + src, rank_bytes,
+                                    cudaMemcpyDeviceToDevice, xs);
+                if (e == cudaSuccess)
+                    e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(vbuf[nxt]) + dst,
+                                        reinterpret_cast<uint8_t*>(vbuf[cur]) + src, rank_bytes,
+                                        cudaMemcpyDeviceToDevice, xs);
+            }
+            if (e == cudaSuccess) e = cudaEventRecord(rr->copied[nxt], xs);
+            if (e != cudaSuccess) return fail_cuda(e, "ring rotation copies");
+        }
+        // Compute step t on the chunks each rank holds now.
+        if (t > 0 && (e = cudaStreamWaitEvent(cs, rr->copied[cur], 0)) != cudaSuccess)
+            return fail_cuda(e, "ring wait");
+        CUtensorMap mk, mv;
+        if ((rc = make_map(&mk, kbuf[cur], P * BH, C, d, ra::fwd::kBN)) != RA_OK) return rc;
+        if ((rc = make_map(&mv, vbuf[cur], P * BH, C, d, ra::fwd::kBN)) != RA_OK) return rc;
+        ra::fwd::FwdParams prm;
+        prm.o = nullptr;
+        prm.o32 = t == 0 ? o_run : o_part;          // step 0 starts the running result
+        prm.lse = t == 0 ? lse : lse_part;
+        prm.S = S;
+        prm.P = P;
+        prm.C = C;
+        prm.causal = causal;
+        prm.pairs_per_chunk = (int)pairs;
+        prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
+        prm.status = st->status;
+        prm.wait_limit_ns = g_wait_limit_ns.load();
+        prm.H = H;
+        prm.group = 1;
+        prm.step = t;
+        prm.BH = BH;
+        {
+            ra::prof::Scope ps(ra::prof::kFwd, cs);
+            if (d == 128)
+                ra::fwd::ring_fwd_kernel<128><<<(unsigned)grid, ra::fwd::kThreads,
+                                                ra::fwd::Cfg<128>::kSmemBytes, cs>>>(mq, mk, mv, prm);
+            else
+                ra::fwd::ring_fwd_kernel<64><<<(unsigned)grid, ra::fwd::kThreads,
+                                               ra::fwd::Cfg<64>::kSmemBytes, cs>>>(mq, mk, mv, prm);
+            ps.done();
+        }
+        if ((e = cudaGetLastError()) != cudaSuccess) return fail_cuda(e, "ring step launch");
+        if ((e = cudaEventRecord(rr->consumed[cur], cs)) != cudaSuccess) return fail_cuda(e, "ring event");
+        if (t > 0) {
+            // fold the step's partial into the running result (in place)
+            rc = attn_merge_partials(o_run, lse, o_part, lse_part, o_run, lse, B, H, S, d, stream);
+            if (rc != RA_OK) return rc;
+        }
+    }
+    // O (fp32, normalized) -> bf16
+    const long long n8 = (long long)((size_t)BH * S * d / 8);
+    long long cb = (n8 + 255) / 256;
+    const long long cap = (long long)st->num_sms * 16;
+    if (cb > cap) cb = cap;
+    ra::dq_convert_kernel<<<(unsigned)cb, 256, 0, cs>>>(o_run, reinterpret_cast<__nv_bfloat16*>(o), n8);
+    if ((e = cudaGetLastError()) != cudaSuccess) return fail_cuda(e, "ring output convert");
+    return RA_OK;
 }
 
 size_t ring_attn_bwd_workspace_size(int B, int H, int S, int d)
