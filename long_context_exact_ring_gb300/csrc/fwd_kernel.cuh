@@ -282,26 +282,31 @@ ring_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, false, true);
+            // Descriptor bases; a k-step only moves the start address -- the
+            // descriptor's low field, address / 16 -- by a constant.
+            const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
+            const uint64_t dk0 = sdesc_sw128(sK, 16, 1024);
+            const uint64_t dv0 = sdesc_sw128(sV, CF::kBoxBytes, 1024);
+            constexpr uint32_t kTile16 = CF::kTileBytes >> 4;
             auto issue_s = [&](int u, int s) {
                 const uint32_t d_tmem = tmem + CF::kColS + 128u * u;
+                const uint64_t dq = dq0 + (uint32_t)u * kTile16;
+                const uint64_t dk = dk0 + (uint32_t)s * kTile16;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * CF::kBoxBytes + (kk & 3) * 32;
-                    const uint64_t a = sdesc_sw128(sQ + u * CF::kTileBytes + off, 16, 1024);
-                    const uint64_t b = sdesc_sw128(sK + s * CF::kTileBytes + off, 16, 1024);
-                    mma_bf16_ss(d_tmem, a, b, idesc_qk, kk > 0 ? 1u : 0u);
+                    constexpr uint32_t kBox16 = CF::kBoxBytes >> 4;
+                    const uint32_t off16 = (kk >> 2) * kBox16 + (kk & 3) * 2;
+                    mma_bf16_ss(d_tmem, dq + off16, dk + off16, idesc_qk, kk > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [&](int u, int s, bool first) {
                 const uint32_t d_tmem = tmem + CF::kColO + (uint32_t)D * u;
                 const uint32_t a_tmem = tmem + CF::kColS + 128u * u;
+                const uint64_t dv = dv0 + (uint32_t)s * kTile16;
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint64_t b = sdesc_sw128(sV + s * CF::kTileBytes + kk * 2048,
-                                                   CF::kBoxBytes, 1024);
-                    mma_bf16_ts(d_tmem, a_tmem + 8u * kk, b, idesc_pv,
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    mma_bf16_ts(d_tmem, a_tmem + 8u * kk, dv + (uint32_t)kk * (2048 >> 4), idesc_pv,
                                 (first && kk == 0) ? 0u : 1u);
-                }
             };
             bool ok = mbar_wait(bar_q, 0, wc) && mbar_wait(bar_k_full(0), 0, wc);
             if (ok) {
@@ -386,9 +391,19 @@ ring_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 for (int c = 0; c < 128; ++c)
                     if (c > lim) s[c] = __float_as_uint(-INFINITY);
             }
-            float mx = __uint_as_float(s[0]);
+            // Row maximum: four independent chains of 3-input maxima.
+            float mq[4];
 #pragma unroll
-            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+            for (int a = 0; a < 4; ++a) mq[a] = __uint_as_float(s[a]);
+#pragma unroll
+            for (int c = 4; c < 124; c += 8) {
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+                    mq[a] = max3f(mq[a], __uint_as_float(s[c + 2 * a]), __uint_as_float(s[c + 2 * a + 1]));
+            }
+            mq[0] = max3f(mq[0], __uint_as_float(s[124]), __uint_as_float(s[125]));
+            mq[1] = max3f(mq[1], __uint_as_float(s[126]), __uint_as_float(s[127]));
+            const float mx = max3f(mq[0], mq[1], fmaxf(mq[2], mq[3]));
             const float m_new = mx * sl2;
             const bool raise = m_new > m_used + kRescaleThreshold;
             float alpha = 1.f;
@@ -397,14 +412,18 @@ ring_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 m_used = m_new;
             }
             const float mb = (m_used == -INFINITY) ? 0.f : m_used;
-            float sum = 0.f;
+            // p = 2^(s * scale * log2 e - m); the row sum in four partials.
+            float sp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < 128; c += 2) {
                 const float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, -mb));
                 const float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), sl2, -mb));
-                sum += p0 + p1;
+                const int a = (c >> 1) & 1;
+                sp[2 * a] += p0;
+                sp[2 * a + 1] += p1;
                 s[c >> 1] = pack_bf16x2(p0, p1);
             }
+            const float sum = (sp[0] + sp[1]) + (sp[2] + sp[3]);
             tmem_st32(tS, *reinterpret_cast<const uint32_t(*)[32]>(&s[0]));
             tmem_st32(tS + 32u, *reinterpret_cast<const uint32_t(*)[32]>(&s[32]));
             l = l * alpha + sum;
