@@ -82,11 +82,27 @@ struct WaitCtl {
     uint64_t limit_ns;
 };
 
+// try_wait that lets the hardware suspend the thread for up to `hint_ns`
+// while the phase is incomplete, so waiting warps do not take issue slots
+// from the warps they share a scheduler with.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0u;
+}
+
 __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtl& w)
 {
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (*w.abort_flag) return false;
         if (globaltimer_ns() - t0 > w.limit_ns) {
             *w.abort_flag = 1;
