@@ -274,69 +274,95 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 for (int s = 0; s < CF::kStages; ++s)
                     if (issued[s] >= 0) mbar_wait(bar_qdo_full(s), (uint32_t)issued[s], drain);
             }
-        } else if (warp == 1 && lane == 0) {
+        } else if (warp == 1) {
             // -------------------------------------------------------- MMA
+            // The whole warp runs the loop converged and waits together; one
+            // elected lane issues each group of MMAs and the commits, which
+            // keeps the code between tcgen05.mma instructions short (the SM
+            // takes one about every 48 cycles).
             constexpr uint32_t idesc_kq = idesc_bf16_f32(kBK, kBQ, false, false);   // S^T, dP^T
             constexpr uint32_t idesc_kd = idesc_bf16_f32(kBK, D, false, true);      // dV, dK
             constexpr uint32_t idesc_qd = idesc_bf16_f32(kBQ, D, true, true);       // dQ tile
+            // A k-step moves a descriptor's start address (its low field,
+            // address / 16) by a constant.
             // C = A(smem, K-major) * B(smem, K-major)^T over the head dim.
             auto mma_kmajor = [&](uint32_t d_tmem, uint32_t sa, uint32_t sb) {
+                const uint64_t da = sdesc_sw128(sa, 16, 1024);
+                const uint64_t db = sdesc_sw128(sb, 16, 1024);
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * CF::kBoxBytes + (kk & 3) * 32;
-                    mma_bf16_ss(d_tmem, sdesc_sw128(sa + off, 16, 1024),
-                                sdesc_sw128(sb + off, 16, 1024), idesc_kq, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off16 = ((kk >> 2) * CF::kBoxBytes + (kk & 3) * 32) >> 4;
+                        mma_bf16_ss(d_tmem, da + off16, db + off16, idesc_kq, kk > 0 ? 1u : 0u);
+                    }
                 }
+                __syncwarp();
             };
             // C += A(TMEM bf16: queries 32g..32g+31 at columns a_tmem + 32g,
             // 16 columns each) * B(smem, queries x D, MN-major).
             auto mma_ts = [&](uint32_t d_tmem, uint32_t a_tmem, uint32_t sb, bool first) {
+                const uint64_t db = sdesc_sw128(sb, CF::kBoxBytes, 1024);
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < kBQ / 16; ++kk)
-                    mma_bf16_ts(d_tmem, a_tmem + (kk >> 1) * 32u + 8u * (kk & 1),
-                                sdesc_sw128(sb + kk * 2048, CF::kBoxBytes, 1024), idesc_kd,
-                                (first && kk == 0) ? 0u : 1u);
+                    for (int kk = 0; kk < kBQ / 16; ++kk)
+                        mma_bf16_ts(d_tmem, a_tmem + (kk >> 1) * 32u + 8u * (kk & 1), db + (uint32_t)kk * (2048 >> 4),
+                                    idesc_kd, (first && kk == 0) ? 0u : 1u);
+                }
+                __syncwarp();
             };
-            bool ok = mbar_wait(bar_kv, 0, wc);
+            // elect.sync picks the lowest lane every time, so each commit comes
+            // from the thread that issued the MMAs it tracks.
+            auto commit = [&](uint32_t bar) {
+                if (elect_one()) mma_commit(bar);
+                __syncwarp();
+            };
+            auto wait_all = [&](uint32_t bar, uint32_t parity) {
+                return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc));
+            };
+            const uint64_t dds0 = sdesc_sw128(sDS, CF::kBoxBytes, 1024);
+            const uint64_t dk0 = sdesc_sw128(sK, CF::kBoxBytes, 1024);
+            bool ok = wait_all(bar_kv, 0);
             for (int n = 0; n < NT && ok; ++n) {
                 const int s = n % CF::kStages;
                 const uint32_t ph = (uint32_t)(n / CF::kStages) & 1u;
                 const uint32_t par = (uint32_t)n & 1u;
-                ok = mbar_wait(bar_qdo_full(s), ph, wc);
-                if (ok && n > 0) ok = mbar_wait(bar_dq_free, par ^ 1u, wc);
+                ok = wait_all(bar_qdo_full(s), ph);
+                if (ok && n > 0) ok = wait_all(bar_dq_free, par ^ 1u);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t qs = sQ + s * CF::kTileBytes;
                 const uint32_t dos = sDO + s * CF::kTileBytes;
                 mma_kmajor(tmem + CF::kColS, sK, qs);
-                mma_commit(bar_s_full);
+                commit(bar_s_full);
                 mma_kmajor(tmem + CF::kColDP, sV, dos);
-                mma_commit(bar_dp_full);
-                ok = mbar_wait(bar_p_ready, par, wc);
+                commit(bar_dp_full);
+                ok = wait_all(bar_p_ready, par);
                 if (!ok) break;
                 tc_fence_after();
                 mma_ts(tmem + CF::kColDV, tmem + CF::kColS, dos, n == 0);
-                ok = mbar_wait(bar_ds_ready, par, wc);
+                ok = wait_all(bar_ds_ready, par);
                 if (!ok) break;
                 tc_fence_after();
                 // dQ tile = dS K into the S region (P^T there was consumed by
                 // dV, issued before).  A is dS^T stored [key][query] (queries
                 // contiguous, MN-major); B is the K tile (d contiguous).
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)
-                    mma_bf16_ss(tmem + CF::kColS, sdesc_sw128(sDS + kk * 2048, CF::kBoxBytes, 1024),
-                                sdesc_sw128(sK + kk * 2048, CF::kBoxBytes, 1024), idesc_qd,
-                                kk > 0 ? 1u : 0u);
-                mma_commit(bar_dq_full);
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        mma_bf16_ss(tmem + CF::kColS, dds0 + (uint32_t)kk * (2048 >> 4), dk0 + (uint32_t)kk * (2048 >> 4),
+                                    idesc_qd, kk > 0 ? 1u : 0u);
+                }
+                __syncwarp();
+                commit(bar_dq_full);
                 mma_ts(tmem + CF::kColDK, tmem + CF::kColDP, qs, n == 0);
-                mma_commit(bar_k_done);
+                commit(bar_k_done);
             }
-            if (ok) mma_commit(bar_kv_final);
-            mma_commit(bar_drain);
+            if (ok) commit(bar_kv_final);
+            commit(bar_drain);
             WaitCtl drain{abort_flag, p.status, 200000000ull};
             volatile int dummy = 0;
             drain.abort_flag = &dummy;
-            mbar_wait(bar_drain, 0, drain);
+            __all_sync(0xffffffffu, mbar_wait(bar_drain, 0, drain));
         } else if (warp == 2 && lane == 0) {
             // ---------------------------------------------------- dQ reducer
             // For each tile: wait until its dQ is staged in the stage's Q /

@@ -21,7 +21,7 @@
 //
 // CTA layout (320 threads):
 //   warp 0      TMA producer: Q tiles once, then K/V tiles in ring order.
-//   warp 1      TMEM allocator and MMA issuer (one elected lane).
+//   warp 1      TMEM allocator and MMA issuer (converged; elect.sync picks the issuing lane).
 //   warps 2-5   softmax / epilogue for query tile 0 (rows 0..127).
 //   warps 6-9   softmax / epilogue for query tile 1 (rows 128..255).
 // The two query tiles share every K/V tile.  TMEM (512 columns):
@@ -279,7 +279,13 @@ ring_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
-        if (lane == 0) {
+        // The whole warp runs this loop converged and waits together; one
+        // elected lane issues each group of MMAs and the commits.  The SM
+        // takes one tcgen05.mma about every 48 cycles against 64 cycles of
+        // work for a 128x128x16 step, so the issuing thread has little slack:
+        // keeping the operands warp-uniform keeps the code around each MMA
+        // short.
+        {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, false, true);
             // Descriptor bases; a k-step only moves the start address -- the
@@ -292,30 +298,45 @@ ring_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 const uint32_t d_tmem = tmem + CF::kColS + 128u * u;
                 const uint64_t dq = dq0 + (uint32_t)u * kTile16;
                 const uint64_t dk = dk0 + (uint32_t)s * kTile16;
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    constexpr uint32_t kBox16 = CF::kBoxBytes >> 4;
-                    const uint32_t off16 = (kk >> 2) * kBox16 + (kk & 3) * 2;
-                    mma_bf16_ss(d_tmem, dq + off16, dk + off16, idesc_qk, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        constexpr uint32_t kBox16 = CF::kBoxBytes >> 4;
+                        const uint32_t off16 = (kk >> 2) * kBox16 + (kk & 3) * 2;
+                        mma_bf16_ss(d_tmem, dq + off16, dk + off16, idesc_qk, kk > 0 ? 1u : 0u);
+                    }
                 }
+                __syncwarp();
             };
             auto issue_pv = [&](int u, int s, bool first) {
                 const uint32_t d_tmem = tmem + CF::kColO + (uint32_t)D * u;
                 const uint32_t a_tmem = tmem + CF::kColS + 128u * u;
                 const uint64_t dv = dv0 + (uint32_t)s * kTile16;
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)
-                    mma_bf16_ts(d_tmem, a_tmem + 8u * kk, dv + (uint32_t)kk * (2048 >> 4), idesc_pv,
-                                (first && kk == 0) ? 0u : 1u);
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        mma_bf16_ts(d_tmem, a_tmem + 8u * kk, dv + (uint32_t)kk * (2048 >> 4), idesc_pv,
+                                    (first && kk == 0) ? 0u : 1u);
+                }
+                __syncwarp();
             };
-            bool ok = mbar_wait(bar_q, 0, wc) && mbar_wait(bar_k_full(0), 0, wc);
+            // elect.sync picks the lowest lane every time, so the commits come
+            // from the thread that issued the MMAs they track.
+            auto commit = [&](uint32_t bar) {
+                if (elect_one()) mma_commit(bar);
+                __syncwarp();
+            };
+            auto wait_all = [&](uint32_t bar, uint32_t parity) {
+                return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc));
+            };
+            bool ok = wait_all(bar_q, 0) && wait_all(bar_k_full(0), 0);
             if (ok) {
                 tc_fence_after();
                 for (int u = 0; u < kQTiles; ++u) {
                     issue_s(u, 0);
-                    mma_commit(bar_s_full(u));
+                    commit(bar_s_full(u));
                 }
-                mma_commit(bar_k_empty(0));
+                commit(bar_k_empty(0));
             }
             for (int n = 0; n < NT && ok; ++n) {
                 const int s = n % CF::kStages;
@@ -323,33 +344,33 @@ ring_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 const int s1 = (n + 1) % CF::kStages;
                 const uint32_t ph1 = (uint32_t)((n + 1) / CF::kStages) & 1u;
                 const bool more = n + 1 < NT;
-                ok = mbar_wait(bar_v_full(s), ph, wc);
+                ok = wait_all(bar_v_full(s), ph);
                 if (!ok) break;
                 for (int u = 0; u < kQTiles && ok; ++u) {
-                    ok = mbar_wait(bar_p_full(u), (uint32_t)n & 1u, wc);
+                    ok = wait_all(bar_p_full(u), (uint32_t)n & 1u);
                     if (!ok) break;
                     tc_fence_after();
                     issue_pv(u, s, n == 0);
-                    if (u == kQTiles - 1) mma_commit(bar_v_empty(s));
+                    if (u == kQTiles - 1) commit(bar_v_empty(s));
                     if (more) {
                         if (u == 0) {
-                            ok = mbar_wait(bar_k_full(s1), ph1, wc);
+                            ok = wait_all(bar_k_full(s1), ph1);
                             if (!ok) break;
                             tc_fence_after();
                         }
                         issue_s(u, s1);
-                        mma_commit(bar_s_full(u));
-                        if (u == kQTiles - 1) mma_commit(bar_k_empty(s1));
+                        commit(bar_s_full(u));
+                        if (u == kQTiles - 1) commit(bar_k_empty(s1));
                     }
                 }
             }
-            if (ok) mma_commit(bar_o_final);
+            if (ok) commit(bar_o_final);
             // Every MMA issued so far must finish before TMEM is released.
-            mma_commit(bar_drain);
+            commit(bar_drain);
             WaitCtl drain{abort_flag, p.status, 200000000ull};
             volatile int dummy = 0;
             drain.abort_flag = &dummy;
-            mbar_wait(bar_drain, 0, drain);
+            __all_sync(0xffffffffu, mbar_wait(bar_drain, 0, drain));
         }
     } else {
         // ------------------------------------------------ softmax + epilogue

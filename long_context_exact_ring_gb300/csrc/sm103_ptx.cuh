@@ -36,6 +36,20 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
 
 __device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31u) == 0u; }
 
+// elect.sync over the full warp: true in exactly one lane (the lowest).  The
+// warp must be converged; tcgen05 issue paths call it so the surrounding code
+// stays warp-uniform.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
