@@ -22,8 +22,10 @@
  * K/V tile.
  *
  * Conventions for every entry point:
- *   - Tensors are contiguous, row-major [B, H, S, d]; LSE and other per-row
- *     vectors are [B, H, S].  ra_bf16 holds raw bfloat16 bits.
+ *   - Tensors are contiguous, row-major [B, H, S, d], except where an
+ *     entry point takes stride arguments (the *_strided calls); LSE and
+ *     other per-row vectors are always contiguous [B, H, S].  ra_bf16 holds
+ *     raw bfloat16 bits.
  *   - All tensor pointers are DEVICE pointers, 16-byte aligned, owned by the
  *     caller.  The library allocates no device memory per call; it keeps one
  *     4-byte status word per device (static device storage).
@@ -91,6 +93,31 @@ int ring_attn_fwd_gqa(const ra_bf16 *q, const ra_bf16 *k, const ra_bf16 *v, ra_b
                       void *stream);
 
 /*
+ * Forward pass over tensors in any row layout ("Training Long-Context Models
+ * Without OOM: Ring Attention", section "Ring Attention Demystified", step 1
+ * splits the sequence of tokens into equal chunks but fixes no memory
+ * layout; sequence-major [B, S, H, d] is the common one in training code).
+ * Computes exactly what ring_attn_fwd_gqa computes (H_kv = H for plain
+ * multi-head attention).
+ *   X_strides  three element strides {batch, head, position} of tensor X:
+ *              row (b, h, s) of X starts at element
+ *              b * X_strides[0] + h * X_strides[1] + s * X_strides[2], and
+ *              its d elements are contiguous.  NULL means the contiguous
+ *              [B, heads, S, d] layout.  [B, S, H, d] storage is
+ *              {S * H * d, d, H * d}.
+ * Every stride of a dimension with more than one index must be a positive
+ * multiple of 8 elements (16 bytes) below 2^35, else RA_ERR_INVALID_ARG.
+ * lse stays contiguous [B, H, S].  The rows of o must not overlap one
+ * another or any input.  The results are bit-identical to the contiguous
+ * entry points on the same values: the layout changes only where rows are
+ * read and written.
+ */
+int ring_attn_fwd_strided(const ra_bf16 *q, const long long *q_strides, const ra_bf16 *k,
+                          const long long *k_strides, const ra_bf16 *v, const long long *v_strides,
+                          ra_bf16 *o, const long long *o_strides, float *lse, int B, int H, int H_kv,
+                          int S, int d, int P, int causal, float scale, void *stream);
+
+/*
  * Bytes of device workspace ring_attn_bwd needs for this shape: an fp32 dQ
  * accumulator [B, H, S, d] plus two fp32 row vectors [B, H, S]
  * (D_r = sum dO_r * O_r and LSE in base 2), each section 256-byte aligned.
@@ -132,6 +159,24 @@ int ring_attn_bwd_gqa(const ra_bf16 *q, const ra_bf16 *k, const ra_bf16 *v, cons
                       const float *lse, const ra_bf16 *dO, ra_bf16 *dq, ra_bf16 *dk, ra_bf16 *dv,
                       int B, int H, int H_kv, int S, int d, int P, int causal, float scale,
                       void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Backward pass over tensors in any row layout: the gradients of
+ * ring_attn_bwd_gqa, with the stride convention of ring_attn_fwd_strided
+ * for each of q, k, v, o, dO, dq, dk and dv (NULL = contiguous).  lse and
+ * the workspace (ring_attn_bwd_workspace_size(B, H, S, d) bytes, 256-byte
+ * aligned) keep their contiguous layouts.  The rows of dq, dk and dv must
+ * not overlap one another or any input.  Results are bit-identical to
+ * ring_attn_bwd_gqa on the same values.
+ */
+int ring_attn_bwd_strided(const ra_bf16 *q, const long long *q_strides, const ra_bf16 *k,
+                          const long long *k_strides, const ra_bf16 *v, const long long *v_strides,
+                          const ra_bf16 *o, const long long *o_strides, const float *lse,
+                          const ra_bf16 *dO, const long long *do_strides, ra_bf16 *dq,
+                          const long long *dq_strides, ra_bf16 *dk, const long long *dk_strides,
+                          ra_bf16 *dv, const long long *dv_strides, int B, int H, int H_kv, int S,
+                          int d, int P, int causal, float scale, void *workspace,
+                          size_t workspace_bytes, void *stream);
 
 /*
  * Size of the fixed device scratch used by ring_attn_bwd_noalloc: 64 MiB per

@@ -28,6 +28,8 @@ EXPORTED = (
     "ring_attn_fwd",
     "ring_attn_fwd_gqa",
     "ring_attn_bwd_gqa",
+    "ring_attn_fwd_strided",
+    "ring_attn_bwd_strided",
     "ring_attn_bwd_workspace_size",
     "ring_attn_fwd_emulated",
     "ring_attn_fwd_emulated_workspace_size",
@@ -72,6 +74,13 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.ring_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
         lib.ring_attn_fwd.restype = i
         lib.ring_attn_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+        llp = ctypes.POINTER(ctypes.c_longlong)
+        lib.ring_attn_fwd_strided.argtypes = [vp, llp, vp, llp, vp, llp, vp, llp, vp, i, i, i, i, i, i,
+                                              i, f, vp]
+        lib.ring_attn_fwd_strided.restype = i
+        lib.ring_attn_bwd_strided.argtypes = [vp, llp, vp, llp, vp, llp, vp, llp, vp, vp, llp, vp, llp,
+                                              vp, llp, vp, llp, i, i, i, i, i, i, i, f, vp, sz, vp]
+        lib.ring_attn_bwd_strided.restype = i
         lib.ring_attn_fwd_gqa.restype = i
         lib.ring_attn_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i,
                                           f, vp, sz, vp]
@@ -135,17 +144,33 @@ def _stream(stream) -> int:
     return int(stream)
 
 
-def _need(t: torch.Tensor, name: str, dtype, shape=None):
+def _need(t: torch.Tensor, name: str, dtype, shape=None, rows_ok: bool = False):
+    """Type, device and shape checks.  rows_ok: any [B, heads, S, d] view whose
+    d-element rows are contiguous is accepted (the library takes its strides);
+    otherwise the tensor must be contiguous."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if not t.is_contiguous():
+    if rows_ok:
+        if t.dim() != 4 or (t.numel() > 0 and t.stride(3) != 1):
+            raise ValueError(f"{name} must be [B, heads, S, d] with contiguous d-element rows")
+    elif not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if shape is not None and tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _strides(t: torch.Tensor):
+    """(batch, head, position) element strides of a [B, heads, S, d] view, as
+    the C array the *_strided entry points take."""
+    return (ctypes.c_longlong * 3)(t.stride(0), t.stride(1), t.stride(2))
+
+
+def _all_contiguous(*ts) -> bool:
+    return all(t.is_contiguous() for t in ts)
 
 
 def _kv_heads(q, k, v):
@@ -156,8 +181,8 @@ def _kv_heads(q, k, v):
     H_kv = k.shape[1]
     if H_kv < 1 or H % H_kv:
         raise ValueError(f"query heads ({H}) must be a multiple of key/value heads ({H_kv})")
-    _need(k, "k", torch.bfloat16, (B, H_kv, S, d))
-    _need(v, "v", torch.bfloat16, (B, H_kv, S, d))
+    _need(k, "k", torch.bfloat16, (B, H_kv, S, d), rows_ok=True)
+    _need(v, "v", torch.bfloat16, (B, H_kv, S, d), rows_ok=True)
     return H_kv
 
 
@@ -165,10 +190,10 @@ def ring_attn_fwd(q, k, v, P: int, causal: bool, scale: float | None = None, *,
                   o=None, lse=None, stream=None):
     """O, LSE = exact ring attention of bf16 [B, H, S, d] q over P chunks.
     k, v are [B, H_kv, S, d]; H_kv < H is grouped-query attention (query
-    head h reads key/value head h // (H / H_kv))."""
-    _need(q, "q", torch.bfloat16)
-    if q.dim() != 4:
-        raise ValueError("q must be [B, H, S, d]")
+    head h reads key/value head h // (H / H_kv)).  q, k, v and o may be
+    strided views whose d-element rows are contiguous -- [B, S, H, d]
+    storage is x.transpose(1, 2) -- and o defaults to q's layout."""
+    _need(q, "q", torch.bfloat16, rows_ok=True)
     B, H, S, d = q.shape
     H_kv = _kv_heads(q, k, v)
     if scale is None:
@@ -177,10 +202,15 @@ def ring_attn_fwd(q, k, v, P: int, causal: bool, scale: float | None = None, *,
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
-    _need(o, "o", torch.bfloat16, q.shape)
+    _need(o, "o", torch.bfloat16, q.shape, rows_ok=True)
     _need(lse, "lse", torch.float32, (B, H, S))
     lib = load_library()
-    if H_kv == H:
+    if not _all_contiguous(q, k, v, o):
+        rc = lib.ring_attn_fwd_strided(q.data_ptr(), _strides(q), k.data_ptr(), _strides(k),
+                                       v.data_ptr(), _strides(v), o.data_ptr(), _strides(o),
+                                       lse.data_ptr(), B, H, H_kv, S, d, int(P), int(bool(causal)),
+                                       float(scale), _stream(stream))
+    elif H_kv == H:
         rc = lib.ring_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                lse.data_ptr(), B, H, S, d, int(P), int(bool(causal)),
                                float(scale), _stream(stream))
@@ -233,29 +263,37 @@ def bwd_workspace_size(B: int, H: int, S: int, d: int) -> int:
 def ring_attn_bwd(q, k, v, o, lse, dO, P: int, causal: bool, scale: float | None = None, *,
                   dq=None, dk=None, dv=None, workspace=None, stream=None):
     """dQ, dK, dV of exact ring attention (P recomputed from the saved LSE).
-    With grouped-query k, v ([B, H_kv, S, d]) dk and dv have that shape."""
-    _need(q, "q", torch.bfloat16)
-    if q.dim() != 4:
-        raise ValueError("q must be [B, H, S, d]")
+    With grouped-query k, v ([B, H_kv, S, d]) dk and dv have that shape.
+    Every bf16 tensor may be a strided view with contiguous d-element rows;
+    dq, dk and dv default to the layouts of q, k and v."""
+    _need(q, "q", torch.bfloat16, rows_ok=True)
     B, H, S, d = q.shape
     H_kv = _kv_heads(q, k, v)
     for t, n in ((o, "o"), (dO, "dO")):
-        _need(t, n, torch.bfloat16, q.shape)
+        _need(t, n, torch.bfloat16, q.shape, rows_ok=True)
     _need(lse, "lse", torch.float32, (B, H, S))
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    _need(dq, "dq", torch.bfloat16, q.shape)
-    _need(dk, "dk", torch.bfloat16, k.shape)
-    _need(dv, "dv", torch.bfloat16, v.shape)
+    _need(dq, "dq", torch.bfloat16, q.shape, rows_ok=True)
+    _need(dk, "dk", torch.bfloat16, k.shape, rows_ok=True)
+    _need(dv, "dv", torch.bfloat16, v.shape, rows_ok=True)
     need = bwd_workspace_size(B, H, S, d)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     _need(workspace, "workspace", torch.uint8)
     lib = load_library()
-    if H_kv == H:
+    if not _all_contiguous(q, k, v, o, dO, dq, dk, dv):
+        rc = lib.ring_attn_bwd_strided(q.data_ptr(), _strides(q), k.data_ptr(), _strides(k),
+                                       v.data_ptr(), _strides(v), o.data_ptr(), _strides(o),
+                                       lse.data_ptr(), dO.data_ptr(), _strides(dO), dq.data_ptr(),
+                                       _strides(dq), dk.data_ptr(), _strides(dk), dv.data_ptr(),
+                                       _strides(dv), B, H, H_kv, S, d, int(P), int(bool(causal)),
+                                       float(scale), workspace.data_ptr(), workspace.numel(),
+                                       _stream(stream))
+    elif H_kv == H:
         rc = lib.ring_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                lse.data_ptr(), dO.data_ptr(), dq.data_ptr(), dk.data_ptr(),
                                dv.data_ptr(), B, H, S, d, int(P), int(bool(causal)),

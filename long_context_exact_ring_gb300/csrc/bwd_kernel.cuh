@@ -49,6 +49,7 @@
 
 #include <cstring>
 
+#include "layout.cuh"
 #include "sm103_ptx.cuh"
 #include "small_kernels.cuh"
 #include "profile.cuh"
@@ -89,14 +90,22 @@ struct BwdParams {
     const float* lse2;      // [B*H, S] LSE * log2(e)   (read directly when rows are not TMA-able)
     const float* Dvec;      // [B*H, S]
     float* dq_acc;          // [B*H*S, D] fp32, pre-zeroed
-    __nv_bfloat16* dk;      // [B*H*S, D]
-    __nv_bfloat16* dv;
+    __nv_bfloat16* dk;      // [B, H_kv, S, D] rows placed by dk_l
+    __nv_bfloat16* dv;      // rows placed by dv_l
+    RowLayout8 dk_l, dv_l;
     int S, P, C, causal, tiles_per_chunk;
     int H, group;           // query heads; query heads per key/value head
     float scale, scale_log2;
+    int rank4;              // bit set: the q (1), k (2), v (4), dO (8) map is 4-D
     uint32_t* status;
     uint64_t wait_limit_ns;
 };
+
+// Kernel parameters (seven tensor maps and BwdParams) are kept within
+// 1 KB: measured on GB300, the same kernel with 1040 bytes of parameters
+// ran about 19 % slower than with 1008, with more warps stalled on long
+// scoreboard dependencies.
+static_assert(7 * sizeof(CUtensorMap) + sizeof(BwdParams) <= 1024, "bwd kernel parameters above 1 KB");
 
 // Query tiles met by key tile kt of chunk j, in ring order: chunks
 // i = j, j+1, ... (mod P), each chunk's tiles ascending; causal keeps
@@ -137,7 +146,12 @@ struct QTiles {
 // kRowTma: the per-query LSE2 / D rows arrive by TMA with the Q / dO tile
 // (needs C % 4 == 0 for 16-byte aligned boxes); otherwise the softmax
 // threads read them from global memory.
-template <int D, bool kRowTma>
+// kStrided: the caller's tensors use general row layouts (tensor maps may be
+// 4-D, dK / dV rows are placed by p.dk_l / p.dv_l); otherwise every tensor
+// is contiguous [B, heads, S, D] and the maps are 3-D over B * heads.  The
+// two are separate instantiations because this kernel's speed proved
+// sensitive to small changes in its generated code.
+template <int D, bool kRowTma, bool kStrided>
 __global__ void __launch_bounds__(kThreads, 1)
 ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
@@ -184,7 +198,7 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     const int items_per_head = p.P * T;
     const int bkv = blockIdx.x / items_per_head;
     const int H_kv = p.H / p.group;
-    const int qh0 = (bkv / H_kv) * p.H + (bkv % H_kv) * p.group;   // first query head of the group
+    const int qh0 = (bkv / H_kv) * p.H + (bkv % H_kv) * p.group;   // first query head of the group (flat b*H + h)
     const int w = blockIdx.x % items_per_head;
     const int chunk_j = w / T;
     const int kt = w % T;
@@ -238,8 +252,16 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             }
             mbar_arrive_expect_tx(bar_kv, 2 * CF::kTileBytes);
             for (int x = 0; x < CF::kBoxes; ++x) {
-                tma_load_3d(sK + x * CF::kBoxBytes, &map_k, bar_kv, 64 * x, k0, bkv);
-                tma_load_3d(sV + x * CF::kBoxBytes, &map_v, bar_kv, 64 * x, k0, bkv);
+                if constexpr (kStrided) {
+                    const int b_idx = bkv / H_kv;
+                    tma_load_rows(sK + x * CF::kBoxBytes, &map_k, bar_kv, 64 * x, k0, bkv - b_idx * H_kv, b_idx,
+                                  H_kv, (p.rank4 & 2) != 0);
+                    tma_load_rows(sV + x * CF::kBoxBytes, &map_v, bar_kv, 64 * x, k0, bkv - b_idx * H_kv, b_idx,
+                                  H_kv, (p.rank4 & 4) != 0);
+                } else {
+                    tma_load_3d(sK + x * CF::kBoxBytes, &map_k, bar_kv, 64 * x, k0, bkv);
+                    tma_load_3d(sV + x * CF::kBoxBytes, &map_v, bar_kv, 64 * x, k0, bkv);
+                }
             }
             int issued[CF::kStages];
             for (int s = 0; s < CF::kStages; ++s) issued[s] = -1;
@@ -254,10 +276,18 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 const int qh = qi.q_head();
                 mbar_arrive_expect_tx(bar_qdo_full(s), kStageTx);
                 for (int x = 0; x < CF::kBoxes; ++x) {
-                    tma_load_3d(sQ + s * CF::kTileBytes + x * CF::kBoxBytes, &map_q,
-                                bar_qdo_full(s), 64 * x, q0, qh);
-                    tma_load_3d(sDO + s * CF::kTileBytes + x * CF::kBoxBytes, &map_do,
-                                bar_qdo_full(s), 64 * x, q0, qh);
+                    if constexpr (kStrided) {
+                        const int b_idx = qh / p.H;
+                        tma_load_rows(sQ + s * CF::kTileBytes + x * CF::kBoxBytes, &map_q, bar_qdo_full(s),
+                                      64 * x, q0, qh - b_idx * p.H, b_idx, p.H, (p.rank4 & 1) != 0);
+                        tma_load_rows(sDO + s * CF::kTileBytes + x * CF::kBoxBytes, &map_do, bar_qdo_full(s),
+                                      64 * x, q0, qh - b_idx * p.H, b_idx, p.H, (p.rank4 & 8) != 0);
+                    } else {
+                        tma_load_3d(sQ + s * CF::kTileBytes + x * CF::kBoxBytes, &map_q,
+                                    bar_qdo_full(s), 64 * x, q0, qh);
+                        tma_load_3d(sDO + s * CF::kTileBytes + x * CF::kBoxBytes, &map_do,
+                                    bar_qdo_full(s), 64 * x, q0, qh);
+                    }
                 }
                 if constexpr (kRowTma) {
                     tma_load_2d(sRow + s * 2 * CF::kRowBytes, &map_lse2, bar_qdo_full(s), q0, qh);
@@ -548,8 +578,13 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             const int col0 = (g & 1) * (D / 2);
             const uint32_t tAcc = tmem_addr(tmem, quarter * 32, (is_dk ? CF::kColDK : CF::kColDV) + col0);
             const float mul = is_dk ? p.scale : 1.f;
-            __nv_bfloat16* out = (is_dk ? p.dk : p.dv) +
-                                 ((size_t)bkv * p.S + (size_t)(key_ok ? kpos : 0)) * D + col0;
+            __nv_bfloat16* out;
+            if constexpr (kStrided) {
+                const int b_idx = bkv / H_kv, h_kv = bkv - b_idx * H_kv, kr = key_ok ? kpos : 0;
+                out = (is_dk ? p.dk : p.dv) + (is_dk ? p.dk_l.row(b_idx, h_kv, kr) : p.dv_l.row(b_idx, h_kv, kr)) + col0;
+            } else {
+                out = (is_dk ? p.dk : p.dv) + ((size_t)bkv * p.S + (size_t)(key_ok ? kpos : 0)) * D + col0;
+            }
 #pragma unroll
             for (int c4 = 0; c4 < D / 64; ++c4) {
                 uint32_t acc[32];
@@ -595,10 +630,14 @@ inline cudaError_t configure_kernels()
     auto set = [&](const void* fn, int bytes) {
         if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     };
-    set((const void*)ring_bwd_kernel<64, true>, Cfg<64>::kSmemBytes);
-    set((const void*)ring_bwd_kernel<64, false>, Cfg<64>::kSmemBytes);
-    set((const void*)ring_bwd_kernel<128, true>, Cfg<128>::kSmemBytes);
-    set((const void*)ring_bwd_kernel<128, false>, Cfg<128>::kSmemBytes);
+    set((const void*)ring_bwd_kernel<64, true, false>, Cfg<64>::kSmemBytes);
+    set((const void*)ring_bwd_kernel<64, false, false>, Cfg<64>::kSmemBytes);
+    set((const void*)ring_bwd_kernel<128, true, false>, Cfg<128>::kSmemBytes);
+    set((const void*)ring_bwd_kernel<128, false, false>, Cfg<128>::kSmemBytes);
+    set((const void*)ring_bwd_kernel<64, true, true>, Cfg<64>::kSmemBytes);
+    set((const void*)ring_bwd_kernel<64, false, true>, Cfg<64>::kSmemBytes);
+    set((const void*)ring_bwd_kernel<128, true, true>, Cfg<128>::kSmemBytes);
+    set((const void*)ring_bwd_kernel<128, false, true>, Cfg<128>::kSmemBytes);
     return e;
 }
 
@@ -606,6 +645,7 @@ struct Launch {
     const void *q, *k, *v, *o, *dO;
     const float* lse;
     void *dq, *dk, *dv;
+    RowLayout lq, lk, lv, lo, ldo, ldq, ldk, ldv;   // row layouts of the caller's tensors
     int B, H, H_kv, S, d, P, causal;
     float scale;
     void* workspace;
@@ -613,7 +653,9 @@ struct Launch {
     int num_sms;
     uint64_t wait_limit_ns;
     cudaStream_t stream;
-    int (*encode)(CUtensorMap*, const void*, int, int, int, int);
+    // map of a bf16 tensor with the given row layout (3-D {d, S, B * heads}
+    // when batch and head fold into one index, else 4-D; *rank4 says which)
+    int (*encode)(CUtensorMap*, const void*, int B, int heads, int S, int d, RowLayout, int rows, bool* rank4);
     int (*encode_rows)(CUtensorMap*, const float*, int, int);
     int (*encode_acc)(CUtensorMap*, float*, int, int, int);
 };
@@ -634,12 +676,22 @@ inline int launch(const Launch& L, cudaError_t* err)
     if (blocks > cap) blocks = cap;
     const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(L.o);
     const __nv_bfloat16* dO = static_cast<const __nv_bfloat16*>(L.dO);
+    auto same = [](const RowLayout& a, const RowLayout& b) { return a.sb == b.sb && a.sh == b.sh && a.ss == b.ss; };
+    const RowLayout cq = normalized(contiguous_layout(L.H, L.S, L.d), L.B, L.H, L.S),
+                    ckv = normalized(contiguous_layout(L.H_kv, L.S, L.d), L.B, L.H_kv, L.S);
+    const bool strided = !(same(L.lq, cq) && same(L.lo, cq) && same(L.ldo, cq) && same(L.ldq, cq) &&
+                           same(L.lk, ckv) && same(L.lv, ckv) && same(L.ldk, ckv) && same(L.ldv, ckv));
     {
         prof::Scope ps(prof::kBwdPrep, L.stream);
-        if (L.d == 128)
-            bwd_prep_kernel<128><<<(unsigned)blocks, 256, 0, L.stream>>>(o, dO, L.lse, Dvec, lse2, (long long)rows);
-        else
-            bwd_prep_kernel<64><<<(unsigned)blocks, 256, 0, L.stream>>>(o, dO, L.lse, Dvec, lse2, (long long)rows);
+        auto prep = [&](auto kern) {
+            kern<<<(unsigned)blocks, 256, 0, L.stream>>>(o, L.lo, dO, L.ldo, L.lse, Dvec, lse2, (long long)rows,
+                                                         L.H, L.S);
+        };
+        if (L.d == 128) {
+            if (strided) prep(bwd_prep_kernel<128, true>); else prep(bwd_prep_kernel<128, false>);
+        } else {
+            if (strided) prep(bwd_prep_kernel<64, true>); else prep(bwd_prep_kernel<64, false>);
+        }
         ps.done();
     }
     e = cudaGetLastError();
@@ -650,8 +702,11 @@ inline int launch(const Launch& L, cudaError_t* err)
     const int BHkv = L.B * L.H_kv;
     const int C = L.S / L.P;
     const bool row_tma = (C % 4) == 0;
-    if (L.encode(&mq, L.q, BH, L.S, L.d, kBQ) || L.encode(&mk, L.k, BHkv, L.S, L.d, kBK) ||
-        L.encode(&mv, L.v, BHkv, L.S, L.d, kBK) || L.encode(&mdo, L.dO, BH, L.S, L.d, kBQ)) {
+    bool r4q = false, r4k = false, r4v = false, r4do = false;
+    if (L.encode(&mq, L.q, L.B, L.H, L.S, L.d, L.lq, kBQ, &r4q) ||
+        L.encode(&mk, L.k, L.B, L.H_kv, L.S, L.d, L.lk, kBK, &r4k) ||
+        L.encode(&mv, L.v, L.B, L.H_kv, L.S, L.d, L.lv, kBK, &r4v) ||
+        L.encode(&mdo, L.dO, L.B, L.H, L.S, L.d, L.ldo, kBQ, &r4do)) {
         *err = cudaErrorInvalidValue;
         return -3;
     }
@@ -671,6 +726,9 @@ inline int launch(const Launch& L, cudaError_t* err)
     prm.dq_acc = dq_acc;
     prm.dk = static_cast<__nv_bfloat16*>(L.dk);
     prm.dv = static_cast<__nv_bfloat16*>(L.dv);
+    prm.dk_l = pack8(L.ldk);
+    prm.dv_l = pack8(L.ldv);
+    prm.rank4 = (r4q ? 1 : 0) | (r4k ? 2 : 0) | (r4v ? 4 : 0) | (r4do ? 8 : 0);
     prm.S = L.S;
     prm.P = L.P;
     prm.C = C;
@@ -686,16 +744,26 @@ inline int launch(const Launch& L, cudaError_t* err)
     {
         prof::Scope ps(prof::kBwdMain, L.stream);
         const dim3 g((unsigned)grid), b(kThreads);
+        auto main_kernel = [&](auto kern, int smem) {
+            kern<<<g, b, smem, L.stream>>>(mq, mk, mv, mdo, mlse, mdv, mdq, prm);
+        };
+        constexpr int s128 = Cfg<128>::kSmemBytes, s64 = Cfg<64>::kSmemBytes;
         if (L.d == 128) {
-            if (row_tma)
-                ring_bwd_kernel<128, true><<<g, b, Cfg<128>::kSmemBytes, L.stream>>>(mq, mk, mv, mdo, mlse, mdv, mdq, prm);
-            else
-                ring_bwd_kernel<128, false><<<g, b, Cfg<128>::kSmemBytes, L.stream>>>(mq, mk, mv, mdo, mlse, mdv, mdq, prm);
+            if (row_tma) {
+                if (strided) main_kernel(ring_bwd_kernel<128, true, true>, s128);
+                else main_kernel(ring_bwd_kernel<128, true, false>, s128);
+            } else {
+                if (strided) main_kernel(ring_bwd_kernel<128, false, true>, s128);
+                else main_kernel(ring_bwd_kernel<128, false, false>, s128);
+            }
         } else {
-            if (row_tma)
-                ring_bwd_kernel<64, true><<<g, b, Cfg<64>::kSmemBytes, L.stream>>>(mq, mk, mv, mdo, mlse, mdv, mdq, prm);
-            else
-                ring_bwd_kernel<64, false><<<g, b, Cfg<64>::kSmemBytes, L.stream>>>(mq, mk, mv, mdo, mlse, mdv, mdq, prm);
+            if (row_tma) {
+                if (strided) main_kernel(ring_bwd_kernel<64, true, true>, s64);
+                else main_kernel(ring_bwd_kernel<64, true, false>, s64);
+            } else {
+                if (strided) main_kernel(ring_bwd_kernel<64, false, true>, s64);
+                else main_kernel(ring_bwd_kernel<64, false, false>, s64);
+            }
         }
         ps.done();
     }
@@ -706,7 +774,14 @@ inline int launch(const Launch& L, cudaError_t* err)
     if (cb > cap) cb = cap;
     {
         prof::Scope ps(prof::kDqConvert, L.stream);
-        dq_convert_kernel<<<(unsigned)cb, 256, 0, L.stream>>>(dq_acc, static_cast<__nv_bfloat16*>(L.dq), n8);
+        auto conv = [&](auto kern) {
+            kern<<<(unsigned)cb, 256, 0, L.stream>>>(dq_acc, static_cast<__nv_bfloat16*>(L.dq), L.ldq, n8, L.H, L.S);
+        };
+        if (L.d == 128) {
+            if (strided) conv(dq_convert_kernel<128, true>); else conv(dq_convert_kernel<128, false>);
+        } else {
+            if (strided) conv(dq_convert_kernel<64, true>); else conv(dq_convert_kernel<64, false>);
+        }
         ps.done();
     }
     e = cudaGetLastError();

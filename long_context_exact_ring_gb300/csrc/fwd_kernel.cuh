@@ -30,6 +30,12 @@
 // P.V MMA straight from TMEM; tcgen05 MMAs of one CTA run in issue order,
 // so the next S = Q K^T (issued after P.V) cannot overwrite P early.
 //
+// Q, K and V are read through tensor maps built from the caller's row
+// layout (layout.cuh) -- 3-D {d, S, B * H} when batch and head fold into
+// one index, else 4-D {d, S, H, B} -- so [B, H, S, d], [B, S, H, d] and
+// other layouts with contiguous d-element rows share one code path; O is
+// stored through the same kind of layout.
+//
 // Online softmax: scores are taken in the log2 domain (x = s * scale *
 // log2 e).  The running maximum used for exponentiation is only raised when
 // the row maximum exceeds it by more than 8 (a factor 256); otherwise the
@@ -38,6 +44,7 @@
 // is saved.
 #pragma once
 
+#include "layout.cuh"
 #include "sm103_ptx.cuh"
 
 namespace ra {
@@ -69,7 +76,9 @@ struct Cfg {
 };
 
 struct FwdParams {
-    __nv_bfloat16* o;       // [B, H, S, D]
+    __nv_bfloat16* o;       // [B, H, S, D] rows placed by `lo`
+    RowLayout lo;
+    int rank4;              // bit set: the q (1), k (2), v (4) map is 4-D
     float* lse;             // [B, H, S]
     int S, P, C;            // sequence, chunks, chunk length
     int H, group;           // query heads; query heads per key/value head
@@ -174,7 +183,6 @@ ring_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     const int q_end = min(q0 + kRowsPerCta, (chunk_i + 1) * p.C);   // rows stored
     // key/value head of this query head (grouped-query attention: query
     // head h reads key/value head h / group)
-    const int bkv = (bh / p.H) * (p.H / p.group) + (bh % p.H) / p.group;
 
     WaitCtl wc{abort_flag, p.status, p.wait_limit_ns};
 
@@ -214,9 +222,7 @@ ring_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         rt.init(p.P, p.C, chunk_i, p.causal, q_end);
         NT = rt.total();
     }
-    // K/V source: the key/value head of the fused ring, or this rank's
-    // receive buffer (rows relative to the chunk start) in step mode.
-    const int kv_head = step_mode ? chunk_i * p.BH + bh : bkv;
+    // K/V rows are relative to the chunk start in step mode.
     const int kv_row0 = step_mode ? rt.j * p.C : 0;
 
     if (NT == 0) {
@@ -235,14 +241,23 @@ ring_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     } else if (warp == 0) {
         // ------------------------------------------------------------ TMA
         if (lane == 0) {
+            // batch and head of this CTA; K/V come from the key/value head
+            // of the fused ring, or from this rank's receive buffer -- a
+            // [P * B, H, C, D] tensor, rows relative to the chunk start -- in
+            // step mode
+            const int b_idx = bh / p.H;
+            const int h_idx = bh - b_idx * p.H;
+            const int kv_h = step_mode ? h_idx : h_idx / p.group;
+            const int kv_b = step_mode ? chunk_i * (p.BH / p.H) + b_idx : b_idx;
+            const int kv_heads = step_mode ? p.H : p.H / p.group;
             tma_prefetch_desc(&map_q);
             tma_prefetch_desc(&map_k);
             tma_prefetch_desc(&map_v);
             mbar_arrive_expect_tx(bar_q, kQTiles * CF::kTileBytes);
             for (int u = 0; u < kQTiles; ++u)
                 for (int x = 0; x < CF::kBoxes; ++x)
-                    tma_load_3d(sQ + u * CF::kTileBytes + x * CF::kBoxBytes, &map_q, bar_q,
-                                64 * x, q0 + kBM * u, bh);
+                    tma_load_rows(sQ + u * CF::kTileBytes + x * CF::kBoxBytes, &map_q, bar_q,
+                                  64 * x, q0 + kBM * u, h_idx, b_idx, p.H, (p.rank4 & 1) != 0);
             int issued_k[CF::kStages], issued_v[CF::kStages];
             for (int s = 0; s < CF::kStages; ++s) issued_k[s] = issued_v[s] = -1;
             bool ok = true;
@@ -254,15 +269,15 @@ ring_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar_k_full(s), CF::kTileBytes);
                 for (int x = 0; x < CF::kBoxes; ++x)
-                    tma_load_3d(sK + s * CF::kTileBytes + x * CF::kBoxBytes, &map_k,
-                                bar_k_full(s), 64 * x, key0 - kv_row0, kv_head);
+                    tma_load_rows(sK + s * CF::kTileBytes + x * CF::kBoxBytes, &map_k,
+                                  bar_k_full(s), 64 * x, key0 - kv_row0, kv_h, kv_b, kv_heads, (p.rank4 & 2) != 0);
                 issued_k[s] = (int)ph;
                 ok = mbar_wait(bar_v_empty(s), ph ^ 1u, wc);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar_v_full(s), CF::kTileBytes);
                 for (int x = 0; x < CF::kBoxes; ++x)
-                    tma_load_3d(sV + s * CF::kTileBytes + x * CF::kBoxBytes, &map_v,
-                                bar_v_full(s), 64 * x, key0 - kv_row0, kv_head);
+                    tma_load_rows(sV + s * CF::kTileBytes + x * CF::kBoxBytes, &map_v,
+                                  bar_v_full(s), 64 * x, key0 - kv_row0, kv_h, kv_b, kv_heads, (p.rank4 & 4) != 0);
                 issued_v[s] = (int)ph;
             }
             if (!ok) {
@@ -470,7 +485,10 @@ ring_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             tc_fence_after();
             const bool store = row < q_end;
             const float inv_l = 1.f / l;
-            const size_t orow_off = ((size_t)bh * p.S + (size_t)(store ? row : 0)) * D;
+            const int srow = store ? row : 0;
+            const int b_idx = bh / p.H;
+            const size_t orow_off = p.o32 ? ((size_t)bh * p.S + (size_t)srow) * D
+                                          : p.lo.row(b_idx, bh - b_idx * p.H, srow);
 #pragma unroll
             for (int c4 = 0; c4 < D / 32; ++c4) {
                 uint32_t o[32];

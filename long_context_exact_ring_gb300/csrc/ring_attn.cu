@@ -96,24 +96,72 @@ int device_state(DeviceState** out)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// 3-D tiled map over a [B*H, S, d] bf16 tensor: box of 64 columns x `rows`
-// rows x 1 head, 128-byte swizzle.  Rows past S read as zero.
-int make_map(CUtensorMap* map, const void* ptr, int BH, int S, int d, int rows)
+// Tiled map over a bf16 tensor of d-element rows placed by `lay`: box of 64
+// columns x `rows` rows of one (batch, head), 128-byte swizzle, rows past S
+// read as zero.  When batch and head fold into one index with a single
+// stride (B == 1, one head, or sb == heads * sh) the map is 3-D
+// {d, S, B * heads}; otherwise it is 4-D {d, S, heads, B}.  *rank4 says
+// which.  A dimension of extent 1 is never stepped along, so an invalid
+// stride there is replaced by a valid placeholder.
+int make_map(CUtensorMap* map, const void* ptr, int B, int heads, int S, int d, ra::RowLayout lay,
+             int rows, bool* rank4)
 {
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)S, (cuuint64_t)BH};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)S * d * 2};
-    cuuint32_t box[3] = {64u, (cuuint32_t)rows, 1u};
-    cuuint32_t estr[3] = {1u, 1u, 1u};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
-                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    auto stride = [&](long long st, int extent) { return (cuuint64_t)((extent > 1 ? st : d) * 2); };
+    long long bh_stride = 0;
+    bool fold = true;
+    if (B == 1) bh_stride = lay.sh;
+    else if (heads == 1) bh_stride = lay.sb;
+    else if (lay.sb == (long long)heads * lay.sh) bh_stride = lay.sh;
+    else fold = false;
+    CUresult r;
+    if (fold) {
+        const int BH = B * heads;
+        cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)S, (cuuint64_t)BH};
+        cuuint64_t strides[2] = {stride(lay.ss, S), stride(bh_stride, BH)};
+        cuuint32_t box[3] = {64u, (cuuint32_t)rows, 1u};
+        cuuint32_t estr[3] = {1u, 1u, 1u};
+        r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)S, (cuuint64_t)heads, (cuuint64_t)B};
+        cuuint64_t strides[3] = {stride(lay.ss, S), stride(lay.sh, heads), stride(lay.sb, B)};
+        cuuint32_t box[4] = {64u, (cuuint32_t)rows, 1u, 1u};
+        cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+        r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (r != CUDA_SUCCESS) {
         std::snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed (%d)",
                       (int)r);
         return RA_ERR_CUDA;
     }
+    *rank4 = !fold;
     return RA_OK;
+}
+
+// A caller's row layout is usable when every dimension of extent > 1 has a
+// positive stride that is a multiple of 8 elements (16 bytes, as the tensor
+// maps and the 16-byte row stores need) and below 2^35 elements (so that
+// stride / 8 fits in 32 bits).  A stride of an extent-1 dimension is never
+// used; it is zeroed so the packed form stays exact.
+bool layout_ok(ra::RowLayout& l, int B, int heads, int S)
+{
+    auto ok = [](long long st, int extent) {
+        return extent <= 1 || (st > 0 && st % 8 == 0 && st < (1ll << 35));
+    };
+    if (!(ok(l.sb, B) && ok(l.sh, heads) && ok(l.ss, S))) return false;
+    l = ra::normalized(l, B, heads, S);
+    return true;
+}
+
+// Layout from a caller's stride triple (batch, head, position), or the
+// contiguous [B, heads, S, d] layout when the pointer is NULL.
+ra::RowLayout layout_from(const long long* strides, int heads, int S, int d)
+{
+    if (!strides) return ra::contiguous_layout(heads, S, d);
+    return ra::RowLayout{strides[0], strides[1], strides[2]};
 }
 
 // 2-D map over a [B*H, S] fp32 row vector: boxes of 128 consecutive rows of
@@ -165,6 +213,7 @@ int check_shape(int B, int H, int S, int d, int P, int causal, float scale)
     if (S % P != 0) return RA_ERR_INVALID_ARG;   // equal contiguous chunks only
     if (d != 64 && d != 128) return RA_ERR_UNSUPPORTED;
     if ((long long)B * H > (1ll << 30)) return RA_ERR_UNSUPPORTED;
+    if ((long long)B * H * S >= (1ll << 31)) return RA_ERR_UNSUPPORTED;   // row indices are 32-bit
     return RA_OK;
 }
 
@@ -245,11 +294,19 @@ int ring_attn_schedule(int P, int causal, int i, int* out_j, int* out_kind, int 
 namespace {
 
 int fwd_impl(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, ra_bf16* o, float* lse, int B,
-             int H, int H_kv, int S, int d, int P, int causal, float scale, void* stream)
+             int H, int H_kv, int S, int d, int P, int causal, float scale, void* stream,
+             const long long* qs = nullptr, const long long* ks = nullptr,
+             const long long* vs = nullptr, const long long* os = nullptr)
 {
     int rc = check_shape(B, H, S, d, P, causal, scale);
     if (rc != RA_OK) return rc;
     if (H_kv < 1 ? H != 0 : (H % H_kv) != 0) return RA_ERR_INVALID_ARG;
+    if ((long long)B * H * S == 0) return RA_OK;   // empty: nothing to launch or read
+    ra::RowLayout lq = layout_from(qs, H, S, d), lk = layout_from(ks, H_kv, S, d),
+                  lv = layout_from(vs, H_kv, S, d), lo = layout_from(os, H, S, d);
+    if (!layout_ok(lq, B, H, S) || !layout_ok(lk, B, H_kv, S) || !layout_ok(lv, B, H_kv, S) ||
+        !layout_ok(lo, B, H, S))
+        return RA_ERR_INVALID_ARG;
     if ((long long)B * H * S == 0) return RA_OK;
     if (!q || !k || !v || !o || !lse) return RA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
@@ -265,12 +322,15 @@ int fwd_impl(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, ra_bf16* o, f
     if (rc != RA_OK) return rc;
     CUtensorMap mq, mk, mv;
     const int BH = B * H;
-    if ((rc = make_map(&mq, q, BH, S, d, ra::fwd::kBM)) != RA_OK) return rc;
-    if ((rc = make_map(&mk, k, B * H_kv, S, d, ra::fwd::kBN)) != RA_OK) return rc;
-    if ((rc = make_map(&mv, v, B * H_kv, S, d, ra::fwd::kBN)) != RA_OK) return rc;
+    bool r4q = false, r4k = false, r4v = false;
+    if ((rc = make_map(&mq, q, B, H, S, d, lq, ra::fwd::kBM, &r4q)) != RA_OK) return rc;
+    if ((rc = make_map(&mk, k, B, H_kv, S, d, lk, ra::fwd::kBN, &r4k)) != RA_OK) return rc;
+    if ((rc = make_map(&mv, v, B, H_kv, S, d, lv, ra::fwd::kBN, &r4v)) != RA_OK) return rc;
 
     ra::fwd::FwdParams prm;
+    prm.rank4 = (r4q ? 1 : 0) | (r4k ? 2 : 0) | (r4v ? 4 : 0);
     prm.o = reinterpret_cast<__nv_bfloat16*>(o);
+    prm.lo = lo;
     prm.lse = lse;
     prm.S = S;
     prm.P = P;
@@ -302,7 +362,7 @@ int fwd_impl(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, ra_bf16* o, f
 int bwd_impl(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, const ra_bf16* o,
              const float* lse, const ra_bf16* dO, ra_bf16* dq, ra_bf16* dk, ra_bf16* dv, int B,
              int H, int H_kv, int S, int d, int P, int causal, float scale, void* workspace,
-             size_t workspace_bytes, void* stream);
+             size_t workspace_bytes, void* stream, const long long* const* strides = nullptr);
 
 // ---------------------------------------------------------------------------
 // Emulated ring: P logical ranks on one GPU
@@ -376,6 +436,15 @@ int ring_attn_fwd_gqa(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, ra_b
     return fwd_impl(q, k, v, o, lse, B, H, H_kv, S, d, P, causal, scale, stream);
 }
 
+int ring_attn_fwd_strided(const ra_bf16* q, const long long* q_strides, const ra_bf16* k,
+                          const long long* k_strides, const ra_bf16* v, const long long* v_strides,
+                          ra_bf16* o, const long long* o_strides, float* lse, int B, int H, int H_kv,
+                          int S, int d, int P, int causal, float scale, void* stream)
+{
+    return fwd_impl(q, k, v, o, lse, B, H, H_kv, S, d, P, causal, scale, stream, q_strides, k_strides,
+                    v_strides, o_strides);
+}
+
 size_t ring_attn_fwd_emulated_workspace_size(int B, int H, int S, int d)
 {
     if (B <= 0 || H <= 0 || S <= 0 || d <= 0) return 0;
@@ -432,7 +501,9 @@ int ring_attn_fwd_emulated(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v,
     if (e != cudaSuccess) return fail_cuda(e, "ring set-up copies");
 
     CUtensorMap mq;
-    if ((rc = make_map(&mq, q, BH, S, d, ra::fwd::kBM)) != RA_OK) return rc;
+    bool r4q = false, r4kv = false;
+    if ((rc = make_map(&mq, q, B, H, S, d, ra::contiguous_layout(H, S, d), ra::fwd::kBM, &r4q)) != RA_OK)
+        return rc;
     for (int t = 0; t < P; ++t) {
         const int cur = t & 1, nxt = cur ^ 1;
         // Rotation for step t + 1 on the interconnect: rank i sends the
@@ -458,10 +529,14 @@ int ring_attn_fwd_emulated(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v,
         if (t > 0 && (e = cudaStreamWaitEvent(cs, rr->copied[cur], 0)) != cudaSuccess)
             return fail_cuda(e, "ring wait");
         CUtensorMap mk, mv;
-        if ((rc = make_map(&mk, kbuf[cur], P * BH, C, d, ra::fwd::kBN)) != RA_OK) return rc;
-        if ((rc = make_map(&mv, vbuf[cur], P * BH, C, d, ra::fwd::kBN)) != RA_OK) return rc;
+        // receive buffers: [P * B, H, C, d], contiguous
+        const ra::RowLayout lbuf = ra::contiguous_layout(H, C, d);
+        if ((rc = make_map(&mk, kbuf[cur], P * B, H, C, d, lbuf, ra::fwd::kBN, &r4kv)) != RA_OK) return rc;
+        if ((rc = make_map(&mv, vbuf[cur], P * B, H, C, d, lbuf, ra::fwd::kBN, &r4kv)) != RA_OK) return rc;
         ra::fwd::FwdParams prm;
+        prm.rank4 = (r4q ? 1 : 0) | (r4kv ? 6 : 0);
         prm.o = nullptr;
+        prm.lo = ra::contiguous_layout(H, S, d);
         prm.o32 = t == 0 ? o_run : o_part;          // step 0 starts the running result
         prm.lse = t == 0 ? lse : lse_part;
         prm.S = S;
@@ -499,7 +574,12 @@ int ring_attn_fwd_emulated(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v,
     long long cb = (n8 + 255) / 256;
     const long long cap = (long long)st->num_sms * 16;
     if (cb > cap) cb = cap;
-    ra::dq_convert_kernel<<<(unsigned)cb, 256, 0, cs>>>(o_run, reinterpret_cast<__nv_bfloat16*>(o), n8);
+    if (d == 128)
+        ra::dq_convert_kernel<128, false><<<(unsigned)cb, 256, 0, cs>>>(o_run, reinterpret_cast<__nv_bfloat16*>(o),
+                                                                ra::contiguous_layout(H, S, d), n8, H, S);
+    else
+        ra::dq_convert_kernel<64, false><<<(unsigned)cb, 256, 0, cs>>>(o_run, reinterpret_cast<__nv_bfloat16*>(o),
+                                                               ra::contiguous_layout(H, S, d), n8, H, S);
     if ((e = cudaGetLastError()) != cudaSuccess) return fail_cuda(e, "ring output convert");
     return RA_OK;
 }
@@ -528,18 +608,44 @@ int ring_attn_bwd_gqa(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, cons
                     workspace_bytes, stream);
 }
 
+int ring_attn_bwd_strided(const ra_bf16* q, const long long* q_strides, const ra_bf16* k,
+                          const long long* k_strides, const ra_bf16* v, const long long* v_strides,
+                          const ra_bf16* o, const long long* o_strides, const float* lse,
+                          const ra_bf16* dO, const long long* do_strides, ra_bf16* dq,
+                          const long long* dq_strides, ra_bf16* dk, const long long* dk_strides,
+                          ra_bf16* dv, const long long* dv_strides, int B, int H, int H_kv, int S,
+                          int d, int P, int causal, float scale, void* workspace,
+                          size_t workspace_bytes, void* stream)
+{
+    const long long* const strides[8] = {q_strides, k_strides, v_strides, o_strides,
+                                         do_strides, dq_strides, dk_strides, dv_strides};
+    return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, H_kv, S, d, P, causal, scale, workspace,
+                    workspace_bytes, stream, strides);
+}
+
 }  // extern "C"
 
 namespace {
 
+// strides: NULL, or 8 stride triples (or NULLs) for q, k, v, o, dO, dq, dk, dv.
 int bwd_impl(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, const ra_bf16* o,
              const float* lse, const ra_bf16* dO, ra_bf16* dq, ra_bf16* dk, ra_bf16* dv, int B,
              int H, int H_kv, int S, int d, int P, int causal, float scale, void* workspace,
-             size_t workspace_bytes, void* stream)
+             size_t workspace_bytes, void* stream, const long long* const* strides)
 {
     int rc = check_shape(B, H, S, d, P, causal, scale);
     if (rc != RA_OK) return rc;
     if (H_kv < 1 ? H != 0 : (H % H_kv) != 0) return RA_ERR_INVALID_ARG;
+    if ((long long)B * H * S == 0) return RA_OK;   // empty: nothing to launch or read
+    auto st_of = [&](int x) { return strides ? strides[x] : nullptr; };
+    ra::RowLayout lq = layout_from(st_of(0), H, S, d), lk = layout_from(st_of(1), H_kv, S, d),
+                  lv = layout_from(st_of(2), H_kv, S, d), lo = layout_from(st_of(3), H, S, d),
+                  ldo = layout_from(st_of(4), H, S, d), ldq = layout_from(st_of(5), H, S, d),
+                  ldk = layout_from(st_of(6), H_kv, S, d), ldv = layout_from(st_of(7), H_kv, S, d);
+    if (!layout_ok(lq, B, H, S) || !layout_ok(lk, B, H_kv, S) || !layout_ok(lv, B, H_kv, S) ||
+        !layout_ok(lo, B, H, S) || !layout_ok(ldo, B, H, S) || !layout_ok(ldq, B, H, S) ||
+        !layout_ok(ldk, B, H_kv, S) || !layout_ok(ldv, B, H_kv, S))
+        return RA_ERR_INVALID_ARG;
     if ((long long)B * H * S == 0) return RA_OK;
     if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)
         return RA_ERR_INVALID_ARG;
@@ -554,15 +660,15 @@ int bwd_impl(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, const ra_bf16
     ra::bwd::Launch L;
     L.q = q; L.k = k; L.v = v; L.o = o; L.lse = lse; L.dO = dO;
     L.dq = dq; L.dk = dk; L.dv = dv;
+    L.lq = lq; L.lk = lk; L.lv = lv; L.lo = lo; L.ldo = ldo; L.ldq = ldq; L.ldk = ldk; L.ldv = ldv;
     L.B = B; L.H = H; L.H_kv = H_kv; L.S = S; L.d = d; L.P = P; L.causal = causal; L.scale = scale;
     L.workspace = workspace;
     L.status = st->status;
     L.num_sms = st->num_sms;
     L.wait_limit_ns = g_wait_limit_ns.load();
     L.stream = static_cast<cudaStream_t>(stream);
-    L.encode = [](CUtensorMap* m, const void* p, int BH, int S_, int d_, int rows) {
-        return make_map(m, p, BH, S_, d_, rows);
-    };
+    L.encode = [](CUtensorMap* m, const void* p, int B_, int heads, int S_, int d_, ra::RowLayout lay,
+                  int rows, bool* rank4) { return make_map(m, p, B_, heads, S_, d_, lay, rows, rank4); };
     L.encode_rows = [](CUtensorMap* m, const float* p, int BH, int S_) {
         return make_row_map(m, p, BH, S_);
     };

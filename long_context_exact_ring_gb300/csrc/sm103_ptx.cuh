@@ -152,6 +152,28 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// 4-D tiled load: coordinates innermost first (column, row, head, batch).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+// Load a box of rows (b, h, row .. row + box) from a map that is either
+// 3-D {d, S, B * heads} (batch and head fold into one index, b * heads + h)
+// or 4-D {d, S, heads, B}.  The host builds the 3-D form whenever the row
+// layout allows it: rank-4 loads measured slower in the backward pass.
+__device__ __forceinline__ void tma_load_rows(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,
+                                              int row, int h, int b, int heads, bool rank4)
+{
+    if (rank4) tma_load_4d(dst, map, bar, x, row, h, b);
+    else tma_load_3d(dst, map, bar, x, row, b * heads + h);
+}
+
 __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                                  int c0, int c1, int c2, uint64_t policy)
 {

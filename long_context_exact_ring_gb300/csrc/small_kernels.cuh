@@ -4,6 +4,7 @@
 //   dq_convert_kernel      fp32 dQ accumulator -> bf16 dQ
 #pragma once
 
+#include "layout.cuh"
 #include "sm103_ptx.cuh"
 
 namespace ra {
@@ -63,22 +64,49 @@ merge_partials_kernel(const float* o_a, const float* lse_a, const float* __restr
 // Backward preparation, one warp per row:
 //   D_r = sum_k dO_rk * O_rk (fp32 accumulate of the bf16 inputs) and
 //   lse2_r = LSE_r * log2(e) (the exponent base the main kernel uses).
-template <int D>
+// Row r = (b H + h) S + s of D and lse2.  kStrided: O and dO rows are
+// placed by their layouts; otherwise both are contiguous [B * H * S, D].
+template <int D, bool kStrided>
 __global__ void __launch_bounds__(256)
-bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
-                const float* __restrict__ lse, float* __restrict__ Dvec, float* __restrict__ lse2,
-                long long rows)
+bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, RowLayout lo, const __nv_bfloat16* __restrict__ dO,
+                RowLayout ldo, const float* __restrict__ lse, float* __restrict__ Dvec,
+                float* __restrict__ lse2, long long rows, int H, int S)
 {
     const long long warp_global = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long warp_count = ((long long)gridDim.x * blockDim.x) >> 5;
     const int lane = threadIdx.x & 31;
     constexpr int kPer = D / 32;   // elements per lane (2 or 4)
-    for (long long r = warp_global; r < rows; r += warp_count) {
-        const size_t base = (size_t)r * D + (size_t)lane * kPer;
+    // Strided: each warp takes a contiguous run of rows and steps (position,
+    // head, batch) along it, so the only divisions are at its start.
+    // Contiguous: warps stride over rows.
+    const long long per = kStrided ? (rows + warp_count - 1) / warp_count : 0;
+    long long r = kStrided ? warp_global * per : warp_global;
+    const long long r_end = kStrided ? min(rows, r + per) : rows;
+    int pos = 0, bi = 0, hi = 0;
+    if constexpr (kStrided) {
+        if (r >= r_end) return;
+        const int bh0 = (int)r / S;          // rows < 2^31 (checked by the host)
+        pos = (int)r - bh0 * S;
+        bi = bh0 / H;
+        hi = bh0 - bi * H;
+    }
+    const size_t col = (size_t)lane * kPer;
+    for (; r < r_end; r += kStrided ? 1 : warp_count) {
+        size_t base_o, base_do;
+        if constexpr (kStrided) {
+            base_o = lo.row(bi, hi, pos) + col;
+            base_do = ldo.row(bi, hi, pos) + col;
+            if (++pos == S) {
+                pos = 0;
+                if (++hi == H) { hi = 0; ++bi; }
+            }
+        } else {
+            base_o = base_do = (size_t)r * D + col;
+        }
         float acc = 0.f;
         if constexpr (kPer == 4) {
-            const uint2 a = *reinterpret_cast<const uint2*>(o + base);
-            const uint2 b = *reinterpret_cast<const uint2*>(dO + base);
+            const uint2 a = *reinterpret_cast<const uint2*>(o + base_o);
+            const uint2 b = *reinterpret_cast<const uint2*>(dO + base_do);
             const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
             const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
 #pragma unroll
@@ -89,8 +117,8 @@ bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __rest
                 acc = fmaf(fa.y, fb.y, acc);
             }
         } else {
-            const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + base);
-            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(dO + base);
+            const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + base_o);
+            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(dO + base_do);
             const float2 fa = __bfloat1622float2(a);
             const float2 fb = __bfloat1622float2(b);
             acc = fmaf(fa.x, fb.x, acc);
@@ -105,12 +133,22 @@ bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __rest
     }
 }
 
-// dQ (fp32 accumulator, already scaled) -> bf16, 8 elements per thread.
+// dQ (fp32 accumulator [B*H*S, D], already scaled) -> bf16, 8 elements per
+// thread; kStrided: the rows are placed by `ldq`, else contiguous.
+template <int D, bool kStrided>
 __global__ void __launch_bounds__(256)
-dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, long long n8)
+dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, RowLayout ldq,
+                  long long n8, int H, int S)
 {
     const long long stride = (long long)gridDim.x * blockDim.x;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
+        size_t dst = (size_t)i * 8;
+        if constexpr (kStrided) {
+            const int r = (int)(i / (D / 8));   // rows < 2^31 (checked by the host)
+            const int col = (int)(i % (D / 8)) * 8;
+            const int bh = r / S;
+            dst = ldq.row(bh / H, bh % H, r - bh * S) + col;
+        }
         const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
         const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
         uint4 out;
@@ -118,7 +156,7 @@ dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
         out.y = pack_bf16x2(a.z, a.w);
         out.z = pack_bf16x2(b.x, b.y);
         out.w = pack_bf16x2(b.z, b.w);
-        reinterpret_cast<uint4*>(dq)[i] = out;
+        *reinterpret_cast<uint4*>(dq + dst) = out;
     }
 }
 

@@ -137,3 +137,29 @@ def test_merge_validates_before_any_launch(lib):
     assert call(out=FAKE * 2) == -1                    # o_out may alias only o_a
     assert call(lout=FAKE * 5) == -1
     assert lib.attn_merge_partials(0, 0, 0, 0, 0, 0, 0, 2, 8, 64, None) == 0
+
+
+def test_strided_entry_points_validate_layouts(lib):
+    ll3 = ctypes.c_longlong * 3
+    B, H, S, d = 1, 2, 256, 128
+    bshd = ll3(S * H * d, d, H * d)
+
+    def fwd(qs=None, os_=None, ptr=FAKE):
+        return lib.ring_attn_fwd_strided(ptr, qs, ptr, bshd, ptr, bshd, ptr, os_, FAKE, B, H, H, S,
+                                         d, 4, 1, ctypes.c_float(0.1), None)
+    assert fwd(qs=ll3(S * H * d, d, H * d + 4)) == -1       # row stride not 16-byte aligned
+    assert fwd(qs=ll3(S * H * d, -d, H * d)) == -1          # negative stride
+    assert fwd(qs=ll3(S * H * d, 0, H * d)) == -1           # zero stride over 2 heads
+    assert fwd(os_=ll3(S * H * d, d, 1 << 37)) == -1        # beyond the stride limit
+    assert fwd(ptr=FAKE + 8, qs=bshd) == -1                 # misaligned pointer
+    # empty shape: nothing is launched or read
+    assert lib.ring_attn_fwd_strided(0, None, 0, None, 0, None, 0, None, 0, 0, H, H, S, d, 4, 1,
+                                     ctypes.c_float(0.1), None) == 0
+    ws = lib.ring_attn_bwd_workspace_size(B, H, S, d)
+
+    def bwd(dks=None):
+        return lib.ring_attn_bwd_strided(FAKE, bshd, FAKE, bshd, FAKE, bshd, FAKE, bshd, FAKE,
+                                         FAKE, bshd, FAKE, bshd, FAKE, dks, FAKE, bshd, B, H, H, S,
+                                         d, 4, 1, ctypes.c_float(0.1), FAKE, ws, None)
+    assert bwd(dks=ll3(S * H * d, d, H * d + 2)) == -1
+    assert bwd(dks=ll3(S * H * d, d, 0)) == -1
