@@ -51,12 +51,12 @@ METRIC = "attention TFLOP/s and tokens/s at 1 GB300 (fwd, fwd+bwd); % of dense B
 # tied to a hash of the kernel's source; once the source changes the figure
 # no longer describes the kernel and the line reports traffic as null.
 KERNEL_TRAFFIC = {
-    "ring_fwd_kernel": {"bytes": 3441366272 + 1144131328,
-                        "sources": ("fwd_kernel.cuh", "sm103_ptx.cuh"),
-                        "sha1": "6d7f57fcf5095517c200c593e095254c5e13c663"},
-    "ring_bwd_kernel": {"bytes": 14228717056 + 8774748672,
-                        "sources": ("bwd_kernel.cuh", "sm103_ptx.cuh"),
-                        "sha1": "1359cbc0b07c6278dc26457c1b0fea0789b335b5"},
+    "ring_fwd_kernel": {"bytes": 3445497088 + 1156870144,
+                        "sources": ("fwd_kernel.cuh", "sm103_ptx.cuh", "layout.cuh"),
+                        "sha1": "ff233dacdab382544cf1c4499e993ad6f3671a41"},
+    "ring_bwd_kernel": {"bytes": 14122141440 + 8661839104,
+                        "sources": ("bwd_kernel.cuh", "sm103_ptx.cuh", "layout.cuh"),
+                        "sha1": "fa5f5030cb5fefa0e90c44fe0140960e2042e33b"},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
