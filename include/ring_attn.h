@@ -93,6 +93,32 @@ int ring_attn_fwd_gqa(const ra_bf16 *q, const ra_bf16 *k, const ra_bf16 *v, ra_b
                       void *stream);
 
 /*
+ * Bytes of device workspace ring_attn_fwd_f32 needs: bf16 copies of q
+ * ([B, H, S, d]) and of k and v ([B, H_kv, S, d]), each 256-byte aligned.
+ * 0 for empty or invalid shapes.
+ */
+size_t ring_attn_fwd_f32_workspace_size(int B, int H, int H_kv, int S, int d);
+
+/*
+ * Forward pass from fp32 inputs (the same method as ring_attn_fwd_gqa;
+ * H_kv = H for plain multi-head attention).
+ *   q        [B, H, S, d] fp32; k, v [B, H_kv, S, d] fp32; contiguous.
+ *   o        [B, H, S, d] fp32 output: O_r normalized, not rounded to bf16.
+ *   lse      [B, H, S] fp32 output (natural log).
+ *   workspace, workspace_bytes  caller-owned device memory of at least
+ *            ring_attn_fwd_f32_workspace_size(B, H, H_kv, S, d) bytes,
+ *            256-byte aligned; it receives the bf16 copies of the inputs.
+ * The inputs are rounded to bf16 (round to nearest even) on the GPU and
+ * multiplied on the bf16 tensor cores with fp32 accumulation, so the result
+ * equals ring_attn_fwd_gqa on the rounded inputs except that O skips the
+ * final bf16 rounding.  o may alias q (q is read before o is written) but
+ * not k or v.  Other arguments and errors as ring_attn_fwd.
+ */
+int ring_attn_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse, int B,
+                      int H, int H_kv, int S, int d, int P, int causal, float scale, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
+/*
  * Forward pass over tensors in any row layout ("Training Long-Context Models
  * Without OOM: Ring Attention", section "Ring Attention Demystified", step 1
  * splits the sequence of tokens into equal chunks but fixes no memory

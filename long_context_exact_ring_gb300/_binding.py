@@ -30,6 +30,8 @@ EXPORTED = (
     "ring_attn_bwd_gqa",
     "ring_attn_fwd_strided",
     "ring_attn_bwd_strided",
+    "ring_attn_fwd_f32",
+    "ring_attn_fwd_f32_workspace_size",
     "ring_attn_bwd_workspace_size",
     "ring_attn_fwd_emulated",
     "ring_attn_fwd_emulated_workspace_size",
@@ -81,6 +83,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.ring_attn_bwd_strided.argtypes = [vp, llp, vp, llp, vp, llp, vp, llp, vp, vp, llp, vp, llp,
                                               vp, llp, vp, llp, i, i, i, i, i, i, i, f, vp, sz, vp]
         lib.ring_attn_bwd_strided.restype = i
+        lib.ring_attn_fwd_f32_workspace_size.argtypes = [i, i, i, i, i]
+        lib.ring_attn_fwd_f32_workspace_size.restype = sz
+        lib.ring_attn_fwd_f32.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, sz, vp]
+        lib.ring_attn_fwd_f32.restype = i
         lib.ring_attn_fwd_gqa.restype = i
         lib.ring_attn_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i,
                                           f, vp, sz, vp]
@@ -219,6 +225,42 @@ def ring_attn_fwd(q, k, v, P: int, causal: bool, scale: float | None = None, *,
                                    lse.data_ptr(), B, H, H_kv, S, d, int(P), int(bool(causal)),
                                    float(scale), _stream(stream))
     _check(rc, "ring_attn_fwd")
+    return o, lse
+
+
+def fwd_f32_workspace_size(B: int, H: int, H_kv: int, S: int, d: int) -> int:
+    return int(load_library().ring_attn_fwd_f32_workspace_size(B, H, H_kv, S, d))
+
+
+def ring_attn_fwd_f32(q, k, v, P: int, causal: bool, scale: float | None = None, *,
+                      o=None, lse=None, workspace=None, stream=None):
+    """O (fp32), LSE of exact ring attention from fp32 [B, H, S, d] q and
+    [B, H_kv, S, d] k, v: the inputs are rounded to bf16 on the GPU and the
+    products accumulate in fp32; O is returned without bf16 rounding."""
+    _need(q, "q", torch.float32)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, S, d]")
+    B, H, S, d = q.shape
+    if k.dim() != 4 or k.shape[0] != B or k.shape[2:] != q.shape[2:]:
+        raise ValueError(f"k has shape {tuple(k.shape)}, expected [B, H_kv, S, d] matching q")
+    H_kv = k.shape[1]
+    _need(k, "k", torch.float32, (B, H_kv, S, d))
+    _need(v, "v", torch.float32, (B, H_kv, S, d))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(o, "o", torch.float32, q.shape)
+    _need(lse, "lse", torch.float32, (B, H, S))
+    need = fwd_f32_workspace_size(B, H, H_kv, S, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _need(workspace, "workspace", torch.uint8)
+    rc = load_library().ring_attn_fwd_f32(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                          lse.data_ptr(), B, H, H_kv, S, d, int(P),
+                                          int(bool(causal)), float(scale), workspace.data_ptr(),
+                                          workspace.numel(), _stream(stream))
+    _check(rc, "ring_attn_fwd_f32")
     return o, lse
 
 
@@ -380,7 +422,7 @@ def set_wait_limit_ns(ns: int) -> None:
 
 
 KERNELS = ("ring_fwd_kernel", "ring_bwd_kernel", "bwd_prep_kernel", "dq_convert_kernel",
-           "merge_partials_kernel")
+           "merge_partials_kernel", "f32_to_bf16_kernel")
 
 
 def profile_enable(on: bool = True) -> None:

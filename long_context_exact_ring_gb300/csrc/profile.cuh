@@ -17,12 +17,13 @@
 namespace ra {
 namespace prof {
 
-enum Kind : int { kFwd = 0, kBwdMain, kBwdPrep, kDqConvert, kMerge, kKinds };
+enum Kind : int { kFwd = 0, kBwdMain, kBwdPrep, kDqConvert, kMerge, kInConvert, kKinds };
 
 inline const char* kind_name(int k)
 {
     static const char* names[kKinds] = {"ring_fwd_kernel", "ring_bwd_kernel", "bwd_prep_kernel",
-                                        "dq_convert_kernel", "merge_partials_kernel"};
+                                        "dq_convert_kernel", "merge_partials_kernel",
+                                        "f32_to_bf16_kernel"};
     return (k >= 0 && k < kKinds) ? names[k] : "";
 }
 

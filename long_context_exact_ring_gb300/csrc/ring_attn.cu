@@ -293,10 +293,12 @@ int ring_attn_schedule(int P, int causal, int i, int* out_j, int* out_kind, int 
 
 namespace {
 
+// o32: when set, O is written in fp32 (contiguous [B, H, S, d]) there and
+// `o` is not used.
 int fwd_impl(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, ra_bf16* o, float* lse, int B,
              int H, int H_kv, int S, int d, int P, int causal, float scale, void* stream,
              const long long* qs = nullptr, const long long* ks = nullptr,
-             const long long* vs = nullptr, const long long* os = nullptr)
+             const long long* vs = nullptr, const long long* os = nullptr, float* o32 = nullptr)
 {
     int rc = check_shape(B, H, S, d, P, causal, scale);
     if (rc != RA_OK) return rc;
@@ -308,6 +310,7 @@ int fwd_impl(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, ra_bf16* o, f
         !layout_ok(lo, B, H, S))
         return RA_ERR_INVALID_ARG;
     if ((long long)B * H * S == 0) return RA_OK;
+    if (o32) o = reinterpret_cast<ra_bf16*>(o32);   // only checked below, never written as bf16
     if (!q || !k || !v || !o || !lse) return RA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
         (reinterpret_cast<uintptr_t>(lse) & 3u))
@@ -341,7 +344,7 @@ int fwd_impl(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, ra_bf16* o, f
     prm.group = H / H_kv;
     prm.step = -1;
     prm.BH = BH;
-    prm.o32 = nullptr;
+    prm.o32 = o32;
     prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
     prm.status = st->status;
     prm.wait_limit_ns = g_wait_limit_ns.load();
@@ -434,6 +437,55 @@ int ring_attn_fwd_gqa(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, ra_b
                       void* stream)
 {
     return fwd_impl(q, k, v, o, lse, B, H, H_kv, S, d, P, causal, scale, stream);
+}
+
+size_t ring_attn_fwd_f32_workspace_size(int B, int H, int H_kv, int S, int d)
+{
+    if (B <= 0 || H <= 0 || H_kv <= 0 || S <= 0 || d <= 0) return 0;
+    const size_t q_elems = (size_t)B * H * S * d, kv_elems = (size_t)B * H_kv * S * d;
+    return ra::bwd::align256(q_elems * 2) + 2 * ra::bwd::align256(kv_elems * 2);
+}
+
+int ring_attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
+                      int H, int H_kv, int S, int d, int P, int causal, float scale, void* workspace,
+                      size_t workspace_bytes, void* stream)
+{
+    int rc = check_shape(B, H, S, d, P, causal, scale);
+    if (rc != RA_OK) return rc;
+    if (H_kv < 1 ? H != 0 : (H % H_kv) != 0) return RA_ERR_INVALID_ARG;
+    if ((long long)B * H * S == 0) return RA_OK;
+    if (!q || !k || !v || !o || !lse || !workspace) return RA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return RA_ERR_INVALID_ARG;
+    if ((const void*)o == (const void*)k || (const void*)o == (const void*)v) return RA_ERR_INVALID_ARG;
+    if (workspace_bytes < ring_attn_fwd_f32_workspace_size(B, H, H_kv, S, d)) return RA_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    if ((rc = device_state(&st)) != RA_OK) return rc;
+    const size_t q_elems = (size_t)B * H * S * d, kv_elems = (size_t)B * H_kv * S * d;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    __nv_bfloat16* qb = reinterpret_cast<__nv_bfloat16*>(ws);
+    __nv_bfloat16* kb = reinterpret_cast<__nv_bfloat16*>(ws + ra::bwd::align256(q_elems * 2));
+    __nv_bfloat16* vb = reinterpret_cast<__nv_bfloat16*>(ws + ra::bwd::align256(q_elems * 2) +
+                                                         ra::bwd::align256(kv_elems * 2));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const long long cap = (long long)st->num_sms * 16;
+    const float* src[3] = {q, k, v};
+    __nv_bfloat16* dst[3] = {qb, kb, vb};
+    const size_t elems[3] = {q_elems, kv_elems, kv_elems};
+    for (int x = 0; x < 3; ++x) {
+        const long long n8 = (long long)(elems[x] / 8);   // d is 64 or 128
+        long long blocks = (n8 + 255) / 256;
+        if (blocks > cap) blocks = cap;
+        ra::prof::Scope ps(ra::prof::kInConvert, s);
+        ra::f32_to_bf16_kernel<<<(unsigned)blocks, 256, 0, s>>>(src[x], dst[x], n8);
+        ps.done();
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return fail_cuda(e, "f32_to_bf16_kernel launch");
+    }
+    return fwd_impl(reinterpret_cast<const ra_bf16*>(qb), reinterpret_cast<const ra_bf16*>(kb),
+                    reinterpret_cast<const ra_bf16*>(vb), nullptr, lse, B, H, H_kv, S, d, P, causal,
+                    scale, stream, nullptr, nullptr, nullptr, nullptr, o);
 }
 
 int ring_attn_fwd_strided(const ra_bf16* q, const long long* q_strides, const ra_bf16* k,

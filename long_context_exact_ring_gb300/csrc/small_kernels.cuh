@@ -160,4 +160,23 @@ dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
     }
 }
 
+// fp32 -> bf16 with round-to-nearest-even, 8 elements per thread and
+// iteration (two 16-byte loads, one 16-byte store); n8 = elements / 8.
+// The fp32-input forward rounds its inputs with it before the bf16 MMAs.
+__global__ void __launch_bounds__(256)
+f32_to_bf16_kernel(const float* __restrict__ in, __nv_bfloat16* __restrict__ out, long long n8)
+{
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
+        const float4 a = reinterpret_cast<const float4*>(in)[2 * i];
+        const float4 b = reinterpret_cast<const float4*>(in)[2 * i + 1];
+        uint4 o;
+        o.x = pack_bf16x2(a.x, a.y);
+        o.y = pack_bf16x2(a.z, a.w);
+        o.z = pack_bf16x2(b.x, b.y);
+        o.w = pack_bf16x2(b.z, b.w);
+        reinterpret_cast<uint4*>(out)[i] = o;
+    }
+}
+
 }  // namespace ra

@@ -163,3 +163,23 @@ def test_strided_entry_points_validate_layouts(lib):
                                          d, 4, 1, ctypes.c_float(0.1), FAKE, ws, None)
     assert bwd(dks=ll3(S * H * d, d, H * d + 2)) == -1
     assert bwd(dks=ll3(S * H * d, d, 0)) == -1
+
+
+def test_f32_forward_validates_before_any_launch(lib):
+    B, H, S, d = 1, 2, 256, 64
+    ws = lib.ring_attn_fwd_f32_workspace_size(B, H, H, S, d)
+    assert ws == 3 * B * H * S * d * 2
+    assert lib.ring_attn_fwd_f32_workspace_size(B, 4, 2, S, d) == (4 + 2 * 2) * S * d * 2
+    assert lib.ring_attn_fwd_f32_workspace_size(0, H, H, S, d) == 0
+
+    def call(q=FAKE, k=FAKE * 2, v=FAKE * 3, o=FAKE * 4, ws_ptr=FAKE * 5, ws_bytes=ws, Hkv=H, S_=S):
+        return lib.ring_attn_fwd_f32(q, k, v, o, FAKE * 6, B, H, Hkv, S_, d, 4, 0,
+                                     ctypes.c_float(0.125), ws_ptr, ws_bytes, None)
+    assert call(ws_bytes=ws - 1) == -1                  # workspace too small
+    assert call(ws_ptr=FAKE * 5 + 16) == -1             # workspace not 256-byte aligned
+    assert call(o=FAKE * 2) == -1                       # o may not alias k
+    assert call(o=FAKE * 3) == -1                       # ... or v
+    assert call(q=FAKE + 8) == -1                       # misaligned
+    assert call(Hkv=3) == -1                            # H not a multiple of H_kv
+    assert call(S_=250) == -1                           # unequal split
+    assert call(S_=0, ws_ptr=0, ws_bytes=0) == 0        # empty: nothing launched
