@@ -73,7 +73,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ring-emulation", action="store_true",
-                    help="skip the emulated-ring forward (P logical ranks, copy-stream rotation)")
+                    help="skip the emulated ring and Ulysses forwards (P logical ranks)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle sample")
     ap.add_argument("--seq", type=int, default=None,
@@ -398,25 +398,25 @@ def main():
                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in.values()),
                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out)}
 
+    def timed(fn, reps=3):
+        """Mean device time of `fn` over `reps` calls after one untimed call."""
+        fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
     # ---- emulated ring: the pages' protocol with P logical ranks ----------
     emu = None
     if not args.no_ring_emulation and inp.get("H_kv", H) == H:
         ws_e = torch.empty(ra.emulated_workspace_size(B, H, S, d), dtype=torch.uint8, device="cuda")
         o_e = torch.empty_like(q)
         lse_e = torch.empty_like(lse)
-
-        def timed(fn, reps=3):
-            fn()
-            torch.cuda.synchronize()
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for _ in range(reps):
-                fn()
-            b.record(stream)
-            torch.cuda.synchronize()
-            return a.elapsed_time(b) / reps
-
         fused = timed(lambda: ra.ring_attn_fwd(q, k, v, P, causal, sc, o=o, lse=lse, stream=stream))
         over = timed(lambda: ra.ring_attn_fwd_emulated(q, k, v, P, causal, sc, overlap=True, o=o_e,
                                                        lse=lse_e, workspace=ws_e, stream=stream))
@@ -431,6 +431,27 @@ def main():
                "rotation_bytes_per_step": step_bytes, "rotations": P - 1,
                "rotation_cost_serialized_ms": serial - over,
                "emulated_overlapped_tflops": f_fwd / (over / 1e3) / 1e12}
+
+    # ---- Ulysses layout path on the same shape: two all-to-alls around ----
+    # ---- full-sequence attention per head group -----------------------------
+    uly = None
+    if not args.no_ring_emulation and H % P == 0 and inp.get("H_kv", H) % P == 0:
+        ws_u = torch.empty(ra.ulysses_workspace_size(B, H, inp["H_kv"], S, d), dtype=torch.uint8,
+                           device="cuda")
+        o_u = torch.empty_like(q)
+        lse_u = torch.empty_like(lse)
+        uly_ms = timed(lambda: ra.ring_attn_fwd_ulysses_emulated(q, k, v, P, causal, sc, o=o_u,
+                                                                 lse=lse_u, workspace=ws_u,
+                                                                 stream=stream))
+        one_chunk = timed(lambda: ra.ring_attn_fwd(q, k, v, 1, causal, sc, o=o_u, lse=lse_u,
+                                                   stream=stream))
+        if ra.check_status() != ra.RA_OK:
+            raise RuntimeError("a kernel reported a bounded-wait timeout in the Ulysses emulation")
+        moved = (q.numel() + k.numel() + v.numel() + q.numel()) * 2 + lse.numel() * 4
+        del ws_u
+        uly = {"pass": "fwd", "P": P, "ulysses_ms": uly_ms, "attention_only_ms": one_chunk,
+               "all_to_all_ms": uly_ms - one_chunk, "all_to_all_bytes": moved,
+               "messages_per_all_to_all": P * P * B, "ulysses_tflops": f_fwd / (uly_ms / 1e3) / 1e12}
 
     # ---- CPU oracle baseline (rank 0, one GPU only) ------------------------
     cpu = None
@@ -454,6 +475,7 @@ def main():
             "cpu_baseline": cpu,
             "e2e": e2e,
             "ring_emulation": emu,
+            "ulysses_emulation": uly,
             "gpu_launches": launches,
             "kernels": {n: {"launches": c, "ms": m} for n, (c, m) in prof.items() if c},
             "clocks": clk,

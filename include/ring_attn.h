@@ -144,6 +144,37 @@ int ring_attn_fwd_strided(const ra_bf16 *q, const long long *q_strides, const ra
                           int S, int d, int P, int causal, float scale, void *stream);
 
 /*
+ * Bytes of device workspace ring_attn_fwd_ulysses_emulated needs: the P
+ * ranks' receive buffers for q and O ([B, H, S, d] bf16 in all), k and v
+ * ([B, H_kv, S, d] bf16) and LSE ([B, H, S] fp32), each 256-byte aligned.
+ * 0 for empty or invalid shapes.
+ */
+size_t ring_attn_fwd_ulysses_workspace_size(int B, int H, int H_kv, int S, int d);
+
+/*
+ * The Ulysses (DeepSpeed) layout path on one GPU, for comparison with the
+ * ring ("Context Parallelism" guide, section 3 "Ulysses (DeepSpeed)", steps
+ * 1-4; "Training Long-Context Models Without OOM: Ring Attention", section
+ * "Ring Attention vs. DeepSpeed Ulysses (All-to-All)").  P logical ranks;
+ * rank i starts with tokens [iC, (i+1)C) of every head of q, k, v
+ * ([B, H, S, d], [B, H_kv, S, d] bf16, contiguous).
+ *   1. all-to-all: rank r receives chunk i of heads [rH/P, (r+1)H/P) (and
+ *      key/value heads [rH_kv/P, (r+1)H_kv/P)) from every rank i -- full
+ *      sequences of H/P heads -- as P^2 B device-to-device copies per tensor;
+ *   2. every rank computes full-sequence attention for its heads (one launch
+ *      of the fused kernel over all ranks, a single chunk);
+ *   3. all-to-all of O and LSE back to the ranks' token chunks.
+ * o, lse as ring_attn_fwd.  Everything runs on `stream` in this order: the
+ * all-to-alls block the compute, as the guide notes.  H and H_kv must be
+ * multiples of P (a rank holds whole heads; the pages' limit on Ulysses
+ * with few key/value heads), else RA_ERR_UNSUPPORTED.  The result equals
+ * ring_attn_fwd_gqa with P = 1 bit for bit.
+ */
+int ring_attn_fwd_ulysses_emulated(const ra_bf16 *q, const ra_bf16 *k, const ra_bf16 *v, ra_bf16 *o,
+                                   float *lse, int B, int H, int H_kv, int S, int d, int P, int causal,
+                                   float scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Bytes of device workspace ring_attn_bwd needs for this shape: an fp32 dQ
  * accumulator [B, H, S, d] plus two fp32 row vectors [B, H, S]
  * (D_r = sum dO_r * O_r and LSE in base 2), each section 256-byte aligned.

@@ -33,6 +33,8 @@ from ._binding import (  # noqa: F401
     emulated_workspace_size,
     ring_attn_fwd_f32,
     fwd_f32_workspace_size,
+    ring_attn_fwd_ulysses_emulated,
+    ulysses_workspace_size,
     ring_schedule,
     set_wait_limit_ns,
     status_string,

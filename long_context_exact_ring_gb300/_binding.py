@@ -32,6 +32,8 @@ EXPORTED = (
     "ring_attn_bwd_strided",
     "ring_attn_fwd_f32",
     "ring_attn_fwd_f32_workspace_size",
+    "ring_attn_fwd_ulysses_emulated",
+    "ring_attn_fwd_ulysses_workspace_size",
     "ring_attn_bwd_workspace_size",
     "ring_attn_fwd_emulated",
     "ring_attn_fwd_emulated_workspace_size",
@@ -87,6 +89,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.ring_attn_fwd_f32_workspace_size.restype = sz
         lib.ring_attn_fwd_f32.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, sz, vp]
         lib.ring_attn_fwd_f32.restype = i
+        lib.ring_attn_fwd_ulysses_workspace_size.argtypes = [i, i, i, i, i]
+        lib.ring_attn_fwd_ulysses_workspace_size.restype = sz
+        lib.ring_attn_fwd_ulysses_emulated.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp,
+                                                       sz, vp]
+        lib.ring_attn_fwd_ulysses_emulated.restype = i
         lib.ring_attn_fwd_gqa.restype = i
         lib.ring_attn_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i,
                                           f, vp, sz, vp]
@@ -261,6 +268,40 @@ def ring_attn_fwd_f32(q, k, v, P: int, causal: bool, scale: float | None = None,
                                           int(bool(causal)), float(scale), workspace.data_ptr(),
                                           workspace.numel(), _stream(stream))
     _check(rc, "ring_attn_fwd_f32")
+    return o, lse
+
+
+def ulysses_workspace_size(B: int, H: int, H_kv: int, S: int, d: int) -> int:
+    return int(load_library().ring_attn_fwd_ulysses_workspace_size(B, H, H_kv, S, d))
+
+
+def ring_attn_fwd_ulysses_emulated(q, k, v, P: int, causal: bool, scale: float | None = None, *,
+                                   o=None, lse=None, workspace=None, stream=None):
+    """The Ulysses layout path with P logical ranks on one GPU: an all-to-all
+    from token chunks to head groups, full-sequence attention per head group,
+    and an all-to-all back.  Needs H and H_kv divisible by P."""
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, S, d]")
+    B, H, S, d = q.shape
+    H_kv = _kv_heads(q, k, v)
+    for t, n in ((k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(o, "o", torch.bfloat16, q.shape)
+    _need(lse, "lse", torch.float32, (B, H, S))
+    need = ulysses_workspace_size(B, H, H_kv, S, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _need(workspace, "workspace", torch.uint8)
+    rc = load_library().ring_attn_fwd_ulysses_emulated(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, H_kv, S, d,
+        int(P), int(bool(causal)), float(scale), workspace.data_ptr(), workspace.numel(),
+        _stream(stream))
+    _check(rc, "ring_attn_fwd_ulysses_emulated")
     return o, lse
 
 

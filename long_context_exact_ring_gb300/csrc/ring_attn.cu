@@ -636,6 +636,114 @@ int ring_attn_fwd_emulated(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v,
     return RA_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// Ulysses layout on one GPU: P logical ranks, two all-to-alls
+// ---------------------------------------------------------------------------
+// ("Context Parallelism" guide, section 3 "Ulysses (DeepSpeed)", steps 1-4;
+// "Training Long-Context Models Without OOM: Ring Attention", section "Ring
+// Attention vs. DeepSpeed Ulysses (All-to-All)".)  Rank i starts with tokens
+// [iC, (i+1)C) of every head.  An all-to-all redistributes by head: rank r
+// receives, from every rank i, the tokens of chunk i for its heads
+// [r H/P, (r+1) H/P) (and key/value heads [r H_kv/P, (r+1) H_kv/P)), so it
+// holds full sequences of H/P heads.  Each rank then computes full-sequence
+// attention for its heads, and a second all-to-all sends each rank's O and
+// LSE rows of chunk i back to rank i.
+//
+// Workspace: the ranks' receive buffers, [P, B, H/P, S, d] for q and O,
+// [P, B, H_kv/P, S, d] for k and v (bf16), and [P, B, H/P, S] fp32 for LSE.
+struct UlyssesLayout {
+    size_t off_q, off_k, off_v, off_o, off_lse, total;
+};
+
+UlyssesLayout ulysses_layout(int B, int H, int H_kv, int S, int d)
+{
+    UlyssesLayout L;
+    const size_t q_elems = (size_t)B * H * S * d, kv_elems = (size_t)B * H_kv * S * d;
+    size_t off = 0;
+    L.off_q = off; off += ra::bwd::align256(q_elems * 2);
+    L.off_k = off; off += ra::bwd::align256(kv_elems * 2);
+    L.off_v = off; off += ra::bwd::align256(kv_elems * 2);
+    L.off_o = off; off += ra::bwd::align256(q_elems * 2);
+    L.off_lse = off; off += ra::bwd::align256((size_t)B * H * S * 4);
+    L.total = off;
+    return L;
+}
+
+// One all-to-all over a [B, heads, S, w]-element tensor held as P sequence
+// shards: block (rank i -> rank r) is chunk i of heads [r hp, (r+1) hp) of
+// every batch.  to_heads: sequence shards (the caller's tensor) -> head
+// shards ([P, B, hp, S, w] buffer); otherwise the way back.  One 2-D copy
+// per (batch, source rank, destination rank): P^2 B messages.
+cudaError_t all_to_all(void* seq, void* heads_buf, int B, int heads, int S, int w, size_t elem, int P,
+                       bool to_heads, cudaStream_t s)
+{
+    const int hp = heads / P, C = S / P;
+    const size_t pitch = (size_t)S * w * elem, width = (size_t)C * w * elem;
+    cudaError_t e = cudaSuccess;
+    for (int r = 0; r < P && e == cudaSuccess; ++r)
+        for (int b = 0; b < B && e == cudaSuccess; ++b)
+            for (int i = 0; i < P && e == cudaSuccess; ++i) {
+                uint8_t* sp = static_cast<uint8_t*>(seq) +
+                              (((size_t)b * heads + (size_t)r * hp) * S + (size_t)i * C) * w * elem;
+                uint8_t* hb = static_cast<uint8_t*>(heads_buf) +
+                              ((((size_t)r * B + b) * hp) * S + (size_t)i * C) * w * elem;
+                e = to_heads ? cudaMemcpy2DAsync(hb, pitch, sp, pitch, width, hp, cudaMemcpyDeviceToDevice, s)
+                             : cudaMemcpy2DAsync(sp, pitch, hb, pitch, width, hp, cudaMemcpyDeviceToDevice, s);
+            }
+    return e;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ring_attn_fwd_ulysses_workspace_size(int B, int H, int H_kv, int S, int d)
+{
+    if (B <= 0 || H <= 0 || H_kv <= 0 || S <= 0 || d <= 0) return 0;
+    return ulysses_layout(B, H, H_kv, S, d).total;
+}
+
+int ring_attn_fwd_ulysses_emulated(const ra_bf16* q, const ra_bf16* k, const ra_bf16* v, ra_bf16* o,
+                                   float* lse, int B, int H, int H_kv, int S, int d, int P, int causal,
+                                   float scale, void* workspace, size_t workspace_bytes, void* stream)
+{
+    int rc = check_shape(B, H, S, d, P, causal, scale);
+    if (rc != RA_OK) return rc;
+    if (H_kv < 1 ? H != 0 : (H % H_kv) != 0) return RA_ERR_INVALID_ARG;
+    if ((long long)B * H * S == 0) return RA_OK;
+    // every rank needs whole heads: P must divide the query and key/value head counts
+    if (H % P != 0 || H_kv % P != 0) return RA_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !o || !lse || !workspace) return RA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return RA_ERR_INVALID_ARG;
+    const UlyssesLayout lay = ulysses_layout(B, H, H_kv, S, d);
+    if (workspace_bytes < lay.total) return RA_ERR_INVALID_ARG;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // step 2: all-to-all on Q, K and V (sequence shards -> head shards)
+    cudaError_t e = all_to_all(const_cast<ra_bf16*>(q), ws + lay.off_q, B, H, S, d, 2, P, true, cs);
+    if (e == cudaSuccess) e = all_to_all(const_cast<ra_bf16*>(k), ws + lay.off_k, B, H_kv, S, d, 2, P, true, cs);
+    if (e == cudaSuccess) e = all_to_all(const_cast<ra_bf16*>(v), ws + lay.off_v, B, H_kv, S, d, 2, P, true, cs);
+    if (e != cudaSuccess) return fail_cuda(e, "Ulysses all-to-all (q, k, v)");
+    // step 3: every rank's full-sequence attention for its heads; the ranks'
+    // buffers together are P * B batches of H / P heads, one launch
+    rc = fwd_impl(reinterpret_cast<const ra_bf16*>(ws + lay.off_q), reinterpret_cast<const ra_bf16*>(ws + lay.off_k),
+                  reinterpret_cast<const ra_bf16*>(ws + lay.off_v), reinterpret_cast<ra_bf16*>(ws + lay.off_o),
+                  reinterpret_cast<float*>(ws + lay.off_lse), P * B, H / P, H_kv / P, S, d, 1, causal, scale,
+                  stream);
+    if (rc != RA_OK) return rc;
+    // step 4: all-to-all on the output (head shards -> sequence shards)
+    e = all_to_all(o, ws + lay.off_o, B, H, S, d, 2, P, false, cs);
+    if (e == cudaSuccess) e = all_to_all(lse, ws + lay.off_lse, B, H, S, 1, 4, P, false, cs);
+    if (e != cudaSuccess) return fail_cuda(e, "Ulysses all-to-all (O, LSE)");
+    return RA_OK;
+}
+
 size_t ring_attn_bwd_workspace_size(int B, int H, int S, int d)
 {
     if (B <= 0 || H <= 0 || S <= 0 || d <= 0) return 0;

@@ -183,3 +183,22 @@ def test_f32_forward_validates_before_any_launch(lib):
     assert call(Hkv=3) == -1                            # H not a multiple of H_kv
     assert call(S_=250) == -1                           # unequal split
     assert call(S_=0, ws_ptr=0, ws_bytes=0) == 0        # empty: nothing launched
+
+
+def test_ulysses_validates_before_any_launch(lib):
+    B, H, S, d = 1, 8, 1024, 128
+    ws = lib.ring_attn_fwd_ulysses_workspace_size(B, H, H, S, d)
+    assert ws == 4 * B * H * S * d * 2 + B * H * S * 4
+    assert lib.ring_attn_fwd_ulysses_workspace_size(B, H, 0, S, d) == 0
+
+    def call(H_=H, Hkv=H, P=4, ws_bytes=ws, ws_ptr=FAKE * 5, q=FAKE):
+        return lib.ring_attn_fwd_ulysses_emulated(q, FAKE * 2, FAKE * 3, FAKE * 4, FAKE * 6, B, H_,
+                                                  Hkv, S, d, P, 1, ctypes.c_float(0.1), ws_ptr,
+                                                  ws_bytes, None)
+    assert call(H_=6, Hkv=6) == -2                      # 6 heads cannot split over 4 ranks
+    assert call(Hkv=2) == -2                            # 2 key/value heads cannot feed 4 ranks
+    assert call(Hkv=3) == -1                            # 8 query heads over 3 key/value heads
+    assert call(ws_bytes=ws - 1) == -1
+    assert call(ws_ptr=FAKE * 5 + 64) == -1             # workspace not 256-byte aligned
+    assert call(q=FAKE + 8) == -1
+    assert call(P=3) == -1                              # 1024 tokens do not split in 3
