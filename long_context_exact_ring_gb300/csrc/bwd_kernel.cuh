@@ -184,7 +184,13 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     const uint32_t bar_kv_final = bar0 + 8u * 11;
     const uint32_t bar_drain = bar0 + 8u * 12;
     const uint32_t bar_k_done = bar0 + 8u * 13;     // dK of the tile done: its Q / dO stage is readable scratch
-    const uint32_t bar_dq_staged = bar0 + 8u * 14;  // the tile's dQ sits in that stage
+    // The dQ tile is staged in two halves: rows 0-63 in the dS buffer (free
+    // once the dQ MMA has read it), rows 64-127 in the tile's Q / dO stage
+    // (free once dK has read it).  The stage then waits for only its own
+    // half's reduction before the next Q / dO load.
+    const uint32_t bar_dqa_staged = bar0 + 8u * 14;  // rows 0-63 sit in the dS buffer
+    const uint32_t bar_dqb_staged = bar0 + 8u * 15;  // rows 64-127 sit in the stage
+    const uint32_t bar_ds_free = bar0 + 8u * 16;     // the dS buffer's half has been read
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + CF::kOffBar + 192);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + CF::kOffBar + 200);
 
@@ -223,7 +229,9 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         mbar_init(bar_kv_final, 1);
         mbar_init(bar_drain, 1);
         mbar_init(bar_k_done, 1);
-        mbar_init(bar_dq_staged, kSoftmaxThreads);
+        mbar_init(bar_dqa_staged, kSoftmaxThreads / 2);
+        mbar_init(bar_dqb_staged, kSoftmaxThreads / 2);
+        mbar_init(bar_ds_free, 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -395,23 +403,33 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             __all_sync(0xffffffffu, mbar_wait(bar_drain, 0, drain));
         } else if (warp == 2 && lane == 0) {
             // ---------------------------------------------------- dQ reducer
-            // For each tile: wait until its dQ is staged in the stage's Q /
-            // dO buffers, add the D / 32 boxes [128 rows x 32 columns] to the
-            // fp32 accumulator, and free the stage once the bulk copies have
-            // read it.  Rows past S are skipped by the TMA; rows past the
-            // chunk end hold exact zeros (their P is masked to 0).
+            // For each tile: add rows 0-63 (D / 32 boxes [64 rows x 32
+            // columns] in the dS buffer) and rows 64-127 (the same boxes'
+            // lower halves in the stage's Q / dO buffers) to the fp32
+            // accumulator, free the dS buffer and then the stage as the bulk
+            // copies finish reading them.  Rows past S are skipped by the
+            // TMA; rows past the chunk end hold exact zeros (their P is
+            // masked to 0).
             tma_prefetch_desc(&map_dq);
             for (int n = 0; n < NT; ++n, qi.next()) {
                 const int s = n % CF::kStages;
-                if (!mbar_wait(bar_dq_staged, (uint32_t)n & 1u, wc)) break;
+                const uint32_t par = (uint32_t)n & 1u;
                 const int q0 = qi.q_start();
+                if (!mbar_wait(bar_dqa_staged, par, wc)) break;
+#pragma unroll
+                for (int b = 0; b < D / 32; ++b)
+                    tma_reduce_add_3d(&map_dq, sDS + (uint32_t)b * 8192u, 32 * b, q0, qi.q_head());
+                bulk_commit_group();
+                if (!mbar_wait(bar_dqb_staged, par, wc)) break;
 #pragma unroll
                 for (int b = 0; b < D / 32; ++b) {
                     const uint32_t src = (b < D / 64 ? sQ : sDO) + s * CF::kTileBytes +
-                                         (b % (D / 64)) * CF::kBoxBytes;
-                    tma_reduce_add_3d(&map_dq, src, 32 * b, q0, qi.q_head());
+                                         (b % (D / 64)) * CF::kBoxBytes + 64u * 128u;
+                    tma_reduce_add_3d(&map_dq, src, 32 * b, q0 + 64, qi.q_head());
                 }
                 bulk_commit_group();
+                bulk_wait_read_1();
+                mbar_arrive(bar_ds_free);
                 bulk_wait_read_all();
                 mbar_arrive(bar_qdo_empty(s));
             }
@@ -524,6 +542,12 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             // dS to shared memory as [key][query] rows, 128-byte swizzle: the
             // 16-byte chunk c of row kr sits at chunk position c ^ (kr & 7);
             // this group's 32 queries are chunks 4 (g & 1) .. +3 of atom g / 2.
+            // The buffer held the previous tile's dQ rows 0-63 until their
+            // reduction read them.
+            if (n > 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar_ds_free, (uint32_t)(n - 1) & 1u, wc));
+                if (!ok) break;
+            }
             uint8_t* ds_row = smem + CF::kOffDS + (g >> 1) * CF::kBoxBytes + kr * 128;
 #pragma unroll
             for (int c = 0; c < 4; ++c)
@@ -549,26 +573,32 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             }
             tc_fence_before();
             mbar_arrive(bar_dq_free);                    // the S region may be reused
-            // Stage the scaled values in this tile's Q / dO buffers once dK
-            // has read them: box b = (kDqCols g) / 32 holds d columns
-            // [32 b, 32 b + 32) as [128 rows][128 bytes], 16-byte chunk c of
-            // row kr at chunk position c ^ (kr & 7).
-            ok = __all_sync(0xffffffffu, mbar_wait(bar_k_done, (uint32_t)n & 1u, wc));
-            if (!ok) break;
+            // Stage the scaled values: box b = (kDqCols g) / 32 holds d
+            // columns [32 b, 32 b + 32), 128 bytes per row, 16-byte chunk c
+            // of row r at chunk position c ^ (r & 7).  Rows 0-63 go to the dS
+            // buffer (boxes of 64 rows, 8 KB) at once: the dQ MMA has read
+            // it.  Rows 64-127 go to this tile's Q / dO buffers once dK has
+            // read them.
             {
                 constexpr int kBoxesQ = D / 64;          // boxes in the Q buffer
                 const int b = (kDqCols * g) / 32;
                 const int c_first = ((kDqCols * g) % 32) / 4;
-                uint8_t* box = smem + (b < kBoxesQ ? CF::kOffQ : CF::kOffDO) + s * CF::kTileBytes +
-                               (b % kBoxesQ) * CF::kBoxBytes + kr * 128;
+                const bool upper = kr < 64;              // uniform over the warp
+                if (!upper) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar_k_done, (uint32_t)n & 1u, wc));
+                    if (!ok) break;
+                }
+                uint8_t* box = upper ? smem + CF::kOffDS + b * 8192 + kr * 128
+                                     : smem + (b < kBoxesQ ? CF::kOffQ : CF::kOffDO) + s * CF::kTileBytes +
+                                           (b % kBoxesQ) * CF::kBoxBytes + kr * 128;
 #pragma unroll
                 for (int c = 0; c < kDqCols / 4; ++c)
                     *reinterpret_cast<float4*>(box + (((c_first + c) ^ (kr & 7)) << 4)) =
                         make_float4(__uint_as_float(a[4 * c]) * sc, __uint_as_float(a[4 * c + 1]) * sc,
                                     __uint_as_float(a[4 * c + 2]) * sc, __uint_as_float(a[4 * c + 3]) * sc);
+                fence_proxy_async_smem();
+                mbar_arrive(upper ? bar_dqa_staged : bar_dqb_staged);
             }
-            fence_proxy_async_smem();
-            mbar_arrive(bar_dq_staged);
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_kv_final, 0, wc));
         if (ok) {

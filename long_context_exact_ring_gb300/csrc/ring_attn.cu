@@ -185,13 +185,14 @@ int make_row_map(CUtensorMap* map, const float* ptr, int BH, int S)
 }
 
 // 3-D map over the fp32 dQ accumulator [B*H, S, d]: boxes of 32 columns x
-// 128 rows x 1 head with 128-byte swizzle, used for TMA reduce-adds.  Rows
-// past S are not written.
+// 64 rows x 1 head with 128-byte swizzle, used for TMA reduce-adds (a
+// 128-row dQ tile is staged and added in two halves).  Rows past S are not
+// written.
 int make_acc_map(CUtensorMap* map, float* ptr, int BH, int S, int d)
 {
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)S, (cuuint64_t)BH};
     cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)S * d * 4};
-    cuuint32_t box[3] = {32u, 128u, 1u};
+    cuuint32_t box[3] = {32u, 64u, 1u};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -462,6 +462,10 @@ __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bul
 // Wait until the bulk operations of this thread no longer read shared memory.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
+// Wait until at most one (the newest) committed bulk group still reads
+// shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
 // Wait until the bulk operations of this thread have fully completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
