@@ -183,13 +183,17 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     const uint32_t bar_dq_free = bar0 + 8u * 10;
     const uint32_t bar_kv_final = bar0 + 8u * 11;
     const uint32_t bar_drain = bar0 + 8u * 12;
-    const uint32_t bar_k_done = bar0 + 8u * 13;     // dK of the tile done: its Q / dO stage is readable scratch
+    // dK of the stage's tile done (its Q has been read): one per stage, since
+    // the MMA can finish the next tile's dK before the reducer frees this
+    // stage, but not the tile after (it needs this stage back).
+    auto bar_k_done = [&](int s) { return bar0 + 8u * (s == 0 ? 13u : 17u); };
     // The dQ tile is staged in two halves: rows 0-63 in the dS buffer (free
-    // once the dQ MMA has read it), rows 64-127 in the tile's Q / dO stage
-    // (free once dK has read it).  The stage then waits for only its own
-    // half's reduction before the next Q / dO load.
+    // once the dQ MMA has read it), rows 64-127 in the tile's dO buffer
+    // (free once dV has read it; dV is issued before dQ).  Neither waits for
+    // dK; the stage is handed back once dK has read Q and the dO half has
+    // been reduced.
     const uint32_t bar_dqa_staged = bar0 + 8u * 14;  // rows 0-63 sit in the dS buffer
-    const uint32_t bar_dqb_staged = bar0 + 8u * 15;  // rows 64-127 sit in the stage
+    const uint32_t bar_dqb_staged = bar0 + 8u * 15;  // rows 64-127 sit in the dO buffer
     const uint32_t bar_ds_free = bar0 + 8u * 16;     // the dS buffer's half has been read
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + CF::kOffBar + 192);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + CF::kOffBar + 200);
@@ -228,7 +232,7 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         mbar_init(bar_dq_free, kSoftmaxThreads);
         mbar_init(bar_kv_final, 1);
         mbar_init(bar_drain, 1);
-        mbar_init(bar_k_done, 1);
+        for (int s = 0; s < CF::kStages; ++s) mbar_init(bar_k_done(s), 1);
         mbar_init(bar_dqa_staged, kSoftmaxThreads / 2);
         mbar_init(bar_dqb_staged, kSoftmaxThreads / 2);
         mbar_init(bar_ds_free, 1);
@@ -393,7 +397,7 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 __syncwarp();
                 commit(bar_dq_full);
                 mma_ts(tmem + CF::kColDK, tmem + CF::kColDP, qs, n == 0);
-                commit(bar_k_done);
+                commit(bar_k_done(s));
             }
             if (ok) commit(bar_kv_final);
             commit(bar_drain);
@@ -404,10 +408,10 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         } else if (warp == 2 && lane == 0) {
             // ---------------------------------------------------- dQ reducer
             // For each tile: add rows 0-63 (D / 32 boxes [64 rows x 32
-            // columns] in the dS buffer) and rows 64-127 (the same boxes'
-            // lower halves in the stage's Q / dO buffers) to the fp32
-            // accumulator, free the dS buffer and then the stage as the bulk
-            // copies finish reading them.  Rows past S are skipped by the
+            // columns] in the dS buffer) and rows 64-127 (the same boxes in
+            // the stage's dO buffer) to the fp32 accumulator; free the dS
+            // buffer, and then the stage once dK has read its Q too, as the
+            // bulk copies finish reading them.  Rows past S are skipped by the
             // TMA; rows past the chunk end hold exact zeros (their P is
             // masked to 0).
             tma_prefetch_desc(&map_dq);
@@ -422,15 +426,14 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 bulk_commit_group();
                 if (!mbar_wait(bar_dqb_staged, par, wc)) break;
 #pragma unroll
-                for (int b = 0; b < D / 32; ++b) {
-                    const uint32_t src = (b < D / 64 ? sQ : sDO) + s * CF::kTileBytes +
-                                         (b % (D / 64)) * CF::kBoxBytes + 64u * 128u;
-                    tma_reduce_add_3d(&map_dq, src, 32 * b, q0 + 64, qi.q_head());
-                }
+                for (int b = 0; b < D / 32; ++b)
+                    tma_reduce_add_3d(&map_dq, sDO + s * CF::kTileBytes + (uint32_t)b * 8192u, 32 * b, q0 + 64,
+                                      qi.q_head());
                 bulk_commit_group();
                 bulk_wait_read_1();
                 mbar_arrive(bar_ds_free);
                 bulk_wait_read_all();
+                if (!mbar_wait(bar_k_done(s), (uint32_t)(n / CF::kStages) & 1u, wc)) break;   // dK read Q
                 mbar_arrive(bar_qdo_empty(s));
             }
             bulk_wait_all();
@@ -574,23 +577,17 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             tc_fence_before();
             mbar_arrive(bar_dq_free);                    // the S region may be reused
             // Stage the scaled values: box b = (kDqCols g) / 32 holds d
-            // columns [32 b, 32 b + 32), 128 bytes per row, 16-byte chunk c
-            // of row r at chunk position c ^ (r & 7).  Rows 0-63 go to the dS
-            // buffer (boxes of 64 rows, 8 KB) at once: the dQ MMA has read
-            // it.  Rows 64-127 go to this tile's Q / dO buffers once dK has
-            // read them.
+            // columns [32 b, 32 b + 32) for 64 rows (8 KB), 128 bytes per
+            // row, 16-byte chunk c of row r at chunk position c ^ (r & 7).
+            // Rows 0-63 go to the dS buffer (the dQ MMA has read it), rows
+            // 64-127 to this tile's dO buffer (dV, issued before dQ, has read
+            // it): both at once.
             {
-                constexpr int kBoxesQ = D / 64;          // boxes in the Q buffer
                 const int b = (kDqCols * g) / 32;
                 const int c_first = ((kDqCols * g) % 32) / 4;
                 const bool upper = kr < 64;              // uniform over the warp
-                if (!upper) {
-                    ok = __all_sync(0xffffffffu, mbar_wait(bar_k_done, (uint32_t)n & 1u, wc));
-                    if (!ok) break;
-                }
                 uint8_t* box = upper ? smem + CF::kOffDS + b * 8192 + kr * 128
-                                     : smem + (b < kBoxesQ ? CF::kOffQ : CF::kOffDO) + s * CF::kTileBytes +
-                                           (b % kBoxesQ) * CF::kBoxBytes + kr * 128;
+                                     : smem + CF::kOffDO + s * CF::kTileBytes + b * 8192 + (kr - 64) * 128;
 #pragma unroll
                 for (int c = 0; c < kDqCols / 4; ++c)
                     *reinterpret_cast<float4*>(box + (((c_first + c) ^ (kr & 7)) << 4)) =
