@@ -56,7 +56,7 @@ KERNEL_TRAFFIC = {
                         "sha1": "3668f7caca854fcf9c730712a7af52dfea77dd67"},
     "ring_bwd_kernel": {"bytes": 14108758784 + 8614416640,
                         "sources": ("bwd_kernel.cuh", "sm103_ptx.cuh", "layout.cuh"),
-                        "sha1": "eecb55ad0b8b5a5d70d94f5970b2f00bc1a9bca4"},
+                        "sha1": "cd65027825d2c5ccc3080088bf0ee7a7a85fc0ce"},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 

@@ -32,16 +32,19 @@
 // other.  The dQ tile reuses the whole S region once dV has consumed P^T
 // (tcgen05 MMAs of a CTA run in issue order); the same warps copy it out of
 // TMEM while dK runs (warp of lane quarter q, warpgroup g: queries
-// 32q..32q+31, d columns [g D/4, (g+1) D/4)) and release the region.  Once
-// dK has consumed the tile's Q / dO stage, they write the scaled fp32 tile
-// into that stage's buffers (128-byte swizzled boxes of 32 columns), and one
-// thread adds it to the fp32 dQ accumulator in global memory with a few TMA
-// bulk reduce-adds before handing the stage back to the producer.
+// 32q..32q+31, d columns [g D/4, (g+1) D/4)) and release the region.  They
+// write the scaled fp32 tile at once as 128-byte swizzled boxes of 32
+// columns x 64 rows: rows 0-63 into the dS buffer (the dQ MMA has read it),
+// rows 64-127 into the tile's dO buffer (dV has read it).  One thread adds
+// both halves to the fp32 dQ accumulator in global memory with TMA bulk
+// reduce-adds, frees the dS buffer, and hands the stage back to the
+// producer once dK has read its Q as well.
 //
 // CTA layout (640 threads, five warpgroups):
 //   WG0    warp 0 TMA producer (K, V once; Q, dO, LSE2, D tiles in ring
-//          order), warp 1 TMEM allocator and MMA issuer, warp 2 dQ reducer
-//          (TMA reduce-add of the staged dQ tiles), warp 3 idle.
+//          order), warp 1 TMEM allocator and MMA issuer (converged; elect.sync
+//          picks the issuing lane), warp 2 dQ reducer (TMA reduce-add of the
+//          staged dQ halves), warp 3 idle.
 //   WG1-4  P^T / dS^T / dQ drain for query columns 32(g-1)..32(g-1)+31
 //          (thread = key row for P and dS, = query row for dQ); epilogue:
 //          WG1-2 write dV, WG3-4 write dK (each half of the d columns).
