@@ -125,3 +125,25 @@ def test_bad_row_stride_is_rejected(ra):
     with pytest.raises(Exception) as e:
         ra.ring_attn_fwd(q, q, q, 2, True, 0.1)
     assert "INVALID_ARG" in str(e.value)
+
+
+@pytest.mark.slow
+def test_bshd_full_size_four_dim_maps(ra):
+    # B = 2 with [B, S, H, d] storage: batch and head cannot share a stride,
+    # so every Q / K / V / dO load goes through the 4-D tensor maps -- at the
+    # peaked workload's full size (2 x 16 heads x 65536 tokens, P = 8)
+    w = workloads.FWD_PEAKED_64K
+    inp = workloads.make(w, device="cuda", keep_fp32=False, backward=True)
+    q, k, v, do = inp["q"], inp["k"], inp["v"], inp["do"]
+    P, causal, sc = inp["P"], inp["causal"], inp["scale"]
+    o_c, lse_c = ra.ring_attn_fwd(q, k, v, P, causal, sc)
+    dq_c, dk_c, dv_c = ra.ring_attn_bwd(q, k, v, o_c, lse_c, do, P, causal, sc)
+    qs, ks, vs, dos = (as_layout(x, "bshd") for x in (q, k, v, do))
+    del q, k, v, do
+    o_s, lse_s = ra.ring_attn_fwd(qs, ks, vs, P, causal, sc)
+    dq_s, dk_s, dv_s = ra.ring_attn_bwd(qs, ks, vs, o_s, lse_s, dos, P, causal, sc)
+    assert ra.check_status() == ra.RA_OK
+    assert o_s.stride() == qs.stride()
+    assert torch.equal(o_s, o_c) and torch.equal(lse_s, lse_c)
+    assert torch.equal(dk_s, dk_c) and torch.equal(dv_s, dv_c)
+    assert_dq_close(dq_s, dq_c)
