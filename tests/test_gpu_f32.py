@@ -65,3 +65,20 @@ def test_f32_output_may_alias_q(ra):
     assert ra.check_status() == ra.RA_OK
     assert got.data_ptr() == buf.data_ptr()
     assert torch.equal(got, want)
+
+
+@pytest.mark.slow
+def test_f32_forward_full_size_matches_bf16_call(ra):
+    # the 128K causal shape (32 heads, P = 4) from fp32 inputs
+    w = workloads.FWD_CAUSAL_128K
+    g = torch.Generator(device="cuda").manual_seed(w.seed)
+    shape = (w.B, w.H, w.S, w.d)
+    q32, k32, v32 = (torch.randn(shape, generator=g, device="cuda") for _ in range(3))
+    sc = 1.0 / w.d ** 0.5
+    o32, lse32 = ra.ring_attn_fwd_f32(q32, k32, v32, w.P, w.causal, sc)
+    q, k, v = (x.to(torch.bfloat16) for x in (q32, k32, v32))
+    del q32, k32, v32
+    o, lse = ra.ring_attn_fwd(q, k, v, w.P, w.causal, sc)
+    assert ra.check_status() == ra.RA_OK
+    assert torch.equal(o32.to(torch.bfloat16), o)
+    assert torch.equal(lse32, lse)
