@@ -353,6 +353,39 @@ const char *ring_attn_last_error(void);
 int ring_attn_set_wait_limit_ns(unsigned long long ns);
 
 /*
+ * Record of the ring order the kernels follow (testing and tracing).
+ *   buf       DEVICE buffer of `capacity` ints, 16-byte aligned, owned by
+ *             the caller; NULL (with capacity 0) turns recording off, which
+ *             is the state at load.
+ * While a buffer is set, every CTA of the forward (ring_fwd_kernel) and
+ * backward (ring_bwd_kernel) kernels launched afterwards on the current
+ * device writes, from its TMA producer thread, the ring visits its tile
+ * stream makes -- one entry each time it enters a new chunk -- into its own
+ * slot of (P + 1) x 8 ints at buf + blockIdx * (P + 1) * 8:
+ *   slot[0..7]        header.  Forward: {b*H + h, query chunk i, first query
+ *                     row of the CTA, number of visits, ring step of a
+ *                     one-step launch or -1, tiles in total, 0, 0}.
+ *                     Backward: {b*H_kv + key/value head, key chunk j, key
+ *                     tile in the chunk, number of visits, query tiles in
+ *                     total, query heads per key/value head, 0, 0}.
+ *   slot[8e .. 8e+7]  visit e = 1 .. visits, in the order made.  Forward:
+ *                     {ring step t, key chunk j, kind, tiles, first key,
+ *                     first key of the last tile, 0, 0}.  Backward: {query
+ *                     chunk i, ring step t = (i - j) mod P, kind, tiles,
+ *                     first query, first query of the last tile, 0, 0}
+ *                     (the tiles of the first query head of a group; the
+ *                     other heads repeat them).
+ *   kind is 0 for the CTA's own chunk (i == j) and 1 for any other.
+ * The order is the one the "Context Parallelism" guide, section 2 "How It
+ * Works", gives: at step t query chunk i meets KV chunk (i - t) mod P, and
+ * causal attention skips chunks j > i.  Slots past `capacity` are not
+ * written.  The setting is per device and process-wide; change it only
+ * while no kernel of this library is running.  Returns RA_ERR_INVALID_ARG
+ * for a misaligned buffer or a NULL/capacity mismatch.
+ */
+int ring_attn_trace_visits(int *buf, long long capacity);
+
+/*
  * Kernel timing.  While enabled, every kernel the library launches is
  * bracketed by a pair of CUDA events on its launch stream.
  * ring_attn_profile_read synchronizes on the recorded events and returns,

@@ -38,4 +38,5 @@ from ._binding import (  # noqa: F401
     ring_schedule,
     set_wait_limit_ns,
     status_string,
+    trace_visits,
 )

@@ -45,6 +45,7 @@ EXPORTED = (
     "ring_attn_status_string",
     "ring_attn_last_error",
     "ring_attn_set_wait_limit_ns",
+    "ring_attn_trace_visits",
     "ring_attn_profile_enable",
     "ring_attn_profile_reset",
     "ring_attn_profile_read",
@@ -122,6 +123,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.ring_attn_last_error.restype = ctypes.c_char_p
         lib.ring_attn_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
         lib.ring_attn_set_wait_limit_ns.restype = i
+        lib.ring_attn_trace_visits.argtypes = [vp, ctypes.c_longlong]
+        lib.ring_attn_trace_visits.restype = i
         lib.ring_attn_profile_enable.argtypes = [i]
         lib.ring_attn_profile_enable.restype = i
         lib.ring_attn_profile_reset.argtypes = []
@@ -460,6 +463,17 @@ def check_status(stream=None) -> int:
 
 def set_wait_limit_ns(ns: int) -> None:
     load_library().ring_attn_set_wait_limit_ns(int(ns))
+
+
+def trace_visits(buf=None) -> None:
+    """Record the ring visits of later forward / backward launches into
+    ``buf`` (an int32 CUDA tensor; see ring_attn_trace_visits in the header
+    for the slot layout), or stop recording with ``None``."""
+    if buf is None:
+        _check(load_library().ring_attn_trace_visits(None, 0), "ring_attn_trace_visits")
+        return
+    _need(buf, "buf", torch.int32)
+    _check(load_library().ring_attn_trace_visits(buf.data_ptr(), buf.numel()), "ring_attn_trace_visits")
 
 
 KERNELS = ("ring_fwd_kernel", "ring_bwd_kernel", "bwd_prep_kernel", "dq_convert_kernel",

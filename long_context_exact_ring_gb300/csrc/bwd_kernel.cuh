@@ -56,6 +56,7 @@
 #include "sm103_ptx.cuh"
 #include "small_kernels.cuh"
 #include "profile.cuh"
+#include "trace.cuh"
 
 namespace ra {
 namespace bwd {
@@ -282,6 +283,8 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             for (int s = 0; s < CF::kStages; ++s) issued[s] = -1;
             bool ok = true;
             constexpr uint32_t kStageTx = 2 * CF::kTileBytes + (kRowTma ? 2 * CF::kRowBytes : 0);
+            int* tr = trace_slot(p.P);   // NULL unless the visit order is being recorded
+            int visits = 0, cur_i = -1;
             for (int n = 0; n < NT; ++n, qi.next()) {
                 const int s = n % CF::kStages;
                 const uint32_t ph = (uint32_t)(n / CF::kStages) & 1u;
@@ -289,6 +292,16 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 if (!ok) break;
                 const int q0 = qi.q_start();
                 const int qh = qi.q_head();
+                if (tr && qi.m == 0) {   // first query head of the group: record each chunk entered
+                    if (qi.i != cur_i && visits < p.P) {
+                        cur_i = qi.i;
+                        ++visits;
+                        trace_put(tr + visits * kTraceInts, qi.i, (qi.i - chunk_j + p.P) % p.P,
+                                  qi.i == chunk_j ? 0 : 1, 0, q0, q0);
+                    }
+                    tr[visits * kTraceInts + 3] += 1;
+                    tr[visits * kTraceInts + 5] = q0;
+                }
                 mbar_arrive_expect_tx(bar_qdo_full(s), kStageTx);
                 for (int x = 0; x < CF::kBoxes; ++x) {
                     if constexpr (kStrided) {
@@ -311,6 +324,7 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 }
                 issued[s] = (int)ph;
             }
+            if (tr) trace_put(tr, bkv, chunk_j, kt, visits, NT, p.group);
             if (!ok) {
                 WaitCtl drain{abort_flag, p.status, 200000000ull};
                 volatile int dummy = 0;

@@ -46,6 +46,7 @@
 
 #include "layout.cuh"
 #include "sm103_ptx.cuh"
+#include "trace.cuh"
 
 namespace ra {
 namespace fwd {
@@ -228,6 +229,10 @@ ring_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     if (NT == 0) {
         // Nothing to attend to in this ring step (causal, chunk above the
         // diagonal): the partial is the merge identity, O = 0, LSE = -inf.
+        if (threadIdx.x == 0) {
+            int* tr = trace_slot(p.P);
+            if (tr) trace_put(tr, bh, chunk_i, q0, 0, p.step, 0);
+        }
         if (warp >= 2) {
             const int u = (warp - 2) >> 2;
             const int row = q0 + kBM * u + (warp & 3) * 32 + lane;
@@ -261,10 +266,17 @@ ring_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             int issued_k[CF::kStages], issued_v[CF::kStages];
             for (int s = 0; s < CF::kStages; ++s) issued_k[s] = issued_v[s] = -1;
             bool ok = true;
+            int* tr = trace_slot(p.P);   // NULL unless the visit order is being recorded
+            int visits = 0;
             for (int n = 0; n < NT && ok; ++n, rt.next()) {
                 const int s = n % CF::kStages;
                 const uint32_t ph = (uint32_t)(n / CF::kStages) & 1u;
                 const int key0 = rt.key_start();
+                if (tr && rt.kt == 0 && visits < p.P) {   // the stream enters chunk j
+                    ++visits;
+                    trace_put(tr + visits * kTraceInts, rt.t, rt.j, rt.j == chunk_i ? 0 : 1, rt.kt_count, key0,
+                              key0 + (rt.kt_count - 1) * kBN);
+                }
                 ok = mbar_wait(bar_k_empty(s), ph ^ 1u, wc);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar_k_full(s), CF::kTileBytes);
@@ -280,6 +292,7 @@ ring_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                                   bar_v_full(s), 64 * x, key0 - kv_row0, kv_h, kv_b, kv_heads, (p.rank4 & 4) != 0);
                 issued_v[s] = (int)ph;
             }
+            if (tr) trace_put(tr, bh, chunk_i, q0, visits, p.step, NT);
             if (!ok) {
                 // Let every copy still in flight land before the CTA exits.
                 WaitCtl drain{abort_flag, p.status, 200000000ull};

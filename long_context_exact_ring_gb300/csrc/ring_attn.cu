@@ -891,6 +891,19 @@ int attn_merge_partials(const float* o_a, const float* lse_a, const float* o_b, 
     return RA_OK;
 }
 
+int ring_attn_trace_visits(int* buf, long long capacity)
+{
+    if (capacity < 0 || (buf == nullptr) != (capacity == 0)) return RA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(buf) & 15u) return RA_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != RA_OK) return rc;
+    const ra::VisitTrace t{buf, capacity};
+    const cudaError_t e = cudaMemcpyToSymbol(ra::g_visit_trace, &t, sizeof(t));
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemcpyToSymbol(visit trace)");
+    return RA_OK;
+}
+
 int ring_attn_profile_enable(int on)
 {
     ra::prof::g_on.store(on ? 1 : 0);

@@ -17,6 +17,9 @@ from .oracle import (  # noqa: F401
     partial,
     bwd,
     bwd_dq_rows,
+    bwd_dkdv_rows,
+    bwd_bf16_rounding_model,
+    naive_fwd_blocked,
     naive_fwd_gqa,
     naive_fwd_rows_gqa,
     bwd_gqa,

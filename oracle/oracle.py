@@ -286,3 +286,161 @@ def attention_flops(B: int, H: int, S: int, d: int, causal: bool) -> int:
     PV, one multiply-add = 2 FLOPs each).  Causal counts pairs c <= r."""
     pairs = S * (S + 1) // 2 if causal else S * S
     return 4 * d * pairs * B * H
+
+
+# ---------------------------------------------------------------------------
+# Whole-head passes with a matrix product as the step (PyTorch, fp64, CPU)
+# ---------------------------------------------------------------------------
+# The C routines above take one dot product at a time: minutes per head at
+# S = 32768, hours at 131072.  The two routines below take the same
+# definition with query rows batched into blocks, so that each row's score
+# vector comes out of one fp64 matrix product (a library primitive); every
+# other step is the definition written out on those vectors, row by row:
+#     s_rc  = scale <q_r, k_c> on the allowed set (c <= r when causal)
+#     M_r   = max_c s_rc,   L_r = sum_c exp(s_rc - M_r),   LSE_r = M_r + ln L_r
+#     P_rc  = exp(s_rc - M_r) / L_r  (= exp(s_rc - LSE_r)),   O_r = sum_c P_rc v_c
+#     dP_rc = <dO_r, v_c>,   D_r = sum_c P_rc dP_rc,   dS_rc = P_rc (dP_rc - D_r)
+#     dK_c  = scale sum_r dS_rc q_r,   dV_c = sum_r P_rc dO_r.
+# The parity tests use them where LSE_r and D_r of every row of a long head
+# are needed (sampled key rows of dK and dV need every query row r >= c).
+
+def _heads64(x):
+    import torch
+    t = torch.as_tensor(np.asarray(x, dtype=np.float64))
+    if t.ndim != 4:
+        raise ValueError("expected [B, H, S, d]")
+    return t
+
+
+def _row_block_scores(Qb, K, r0, causal, scale):
+    """Scores of query rows r0 .. r0 + len(Qb) - 1 against keys 0 .. len(K) - 1,
+    with the keys c > r set to -inf when causal."""
+    import torch
+    s = (Qb @ K.T) * scale
+    if causal:
+        r = torch.arange(r0, r0 + Qb.shape[0]).unsqueeze(1)
+        c = torch.arange(K.shape[0]).unsqueeze(0)
+        s.masked_fill_(c > r, float("-inf"))
+    return s
+
+
+def naive_fwd_blocked(q, k, v, causal: bool, scale: float, block: int = 256):
+    """The definition over whole [B, H, S, d] tensors, query rows in blocks
+    -> (O, LSE) as numpy float64."""
+    import torch
+    Q, K, V = _heads64(q), _heads64(k), _heads64(v)
+    B, H, S, d = Q.shape
+    O = torch.empty_like(Q)
+    LSE = torch.empty((B, H, S), dtype=torch.float64)
+    for b in range(B):
+        for h in range(H):
+            for r0 in range(0, S, block):
+                r1 = min(S, r0 + block)
+                kmax = r1 if causal else S          # keys past the block's last row are masked
+                s = _row_block_scores(Q[b, h, r0:r1], K[b, h, :kmax], r0, causal, scale)
+                M = s.max(dim=1, keepdim=True).values
+                e = torch.exp(s - M)
+                L = e.sum(dim=1, keepdim=True)
+                O[b, h, r0:r1] = (e / L) @ V[b, h, :kmax]
+                LSE[b, h, r0:r1] = (M + torch.log(L)).squeeze(1)
+    return O.numpy(), LSE.numpy()
+
+
+def bwd_dkdv_rows(q, k, v, dO, causal: bool, scale: float, keys, block: int = 256):
+    """dK and dV at chosen key positions of ONE head ([1, 1, S, d] inputs),
+    with LSE_r and D_r of every query row computed here from the definition.
+    Returns (dK [n, d], dV [n, d], LSE [S], D [S]) as numpy float64."""
+    import torch
+    Q, K, V, dOt = (_heads64(x) for x in (q, k, v, dO))
+    if Q.shape[:2] != (1, 1):
+        raise ValueError("one head at a time: inputs shaped [1, 1, S, d]")
+    Q, K, V, dOt = Q[0, 0], K[0, 0], V[0, 0], dOt[0, 0]
+    S, d = Q.shape
+    keys = torch.as_tensor(np.asarray(keys, dtype=np.int64))
+    if keys.numel() and (int(keys.min()) < 0 or int(keys.max()) >= S):
+        raise ValueError("key index out of range")
+    dK = torch.zeros((keys.numel(), d), dtype=torch.float64)
+    dV = torch.zeros((keys.numel(), d), dtype=torch.float64)
+    LSE = torch.empty(S, dtype=torch.float64)
+    Dv = torch.empty(S, dtype=torch.float64)
+    for r0 in range(0, S, block):
+        r1 = min(S, r0 + block)
+        kmax = r1 if causal else S
+        s = _row_block_scores(Q[r0:r1], K[:kmax], r0, causal, scale)
+        M = s.max(dim=1, keepdim=True).values
+        e = torch.exp(s - M)
+        L = e.sum(dim=1, keepdim=True)
+        Pm = e / L
+        dP = dOt[r0:r1] @ V[:kmax].T
+        D = (Pm * dP).sum(dim=1, keepdim=True)
+        LSE[r0:r1] = (M + torch.log(L)).squeeze(1)
+        Dv[r0:r1] = D.squeeze(1)
+        sel = torch.nonzero(keys < kmax).squeeze(1)     # keys these rows can see
+        if sel.numel() == 0:
+            continue
+        cols = keys[sel]
+        Psel = Pm[:, cols]
+        dS = Psel * (dP[:, cols] - D)
+        dK[sel] += scale * (dS.T @ Q[r0:r1])
+        dV[sel] += Psel.T @ dOt[r0:r1]
+    return dK.numpy(), dV.numpy(), LSE.numpy(), Dv.numpy()
+
+
+# ---------------------------------------------------------------------------
+# Rounding model of a bf16-storage backward (PyTorch, fp64, CPU)
+# ---------------------------------------------------------------------------
+# The plain derivative above is exact; a backward whose tensors are stored in
+# bf16 cannot reach it.  This routine evaluates the same derivative in fp64
+# with an exact bf16 rounding (round to nearest even) applied at the four
+# places where the stored format is bf16:
+#   O      -- the forward's output, which D_r = <dO_r, O_r> is formed from
+#             (activations kept for the backward pass, "Training
+#             Long-Context Models Without OOM: Ring Attention", section
+#             "Diagnosing the Sequence-Length OOM");
+#   P      -- the probabilities entering dV = P^T dO;
+#   dS     -- entering dQ = scale dS K and dK = scale dS^T Q;
+#   dQ, dK, dV -- the outputs.
+# Its distance from the exact derivative is the error that storage alone
+# causes; the parity tests of stress inputs allow that much on top of the
+# gradient tolerance.  With round_bf16=False every rounding is the identity
+# and the routine is the plain derivative again.
+
+def _bf16_rne(t):
+    """fp64 -> nearest bf16 value (ties to even), returned as fp64.  Done on
+    the bit pattern of the fp32 value nearest t; fp64 inputs here are bf16
+    values times O(1) factors, so the fp32 step never decides a tie."""
+    import torch
+    f = t.to(torch.float32).contiguous()
+    bits = f.view(torch.int32).to(torch.int64) & 0xFFFFFFFF
+    lsb = (bits >> 16) & 1
+    rounded = ((bits + 0x7FFF + lsb) >> 16) << 16
+    out = (rounded & 0xFFFFFFFF).to(torch.int64)
+    out = torch.where(out >= 2 ** 31, out - 2 ** 32, out).to(torch.int32)
+    return out.view(torch.float32).to(torch.float64)
+
+
+def bwd_bf16_rounding_model(q, k, v, dO, causal: bool, scale: float, round_bf16: bool = True):
+    """(dQ, dK, dV) of whole [B, H, S, d] tensors with bf16 storage of O, P,
+    dS and the outputs (see above) -> numpy float64.  Small shapes only
+    (S x S matrices per head)."""
+    import torch
+    Q, K, V, dOt = (_heads64(x) for x in (q, k, v, dO))
+    B, H, S, d = Q.shape
+    rnd = _bf16_rne if round_bf16 else (lambda t: t)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(Q), torch.empty_like(Q)
+    mask = torch.triu(torch.ones(S, S, dtype=torch.bool), diagonal=1) if causal else None
+    for b in range(B):
+        for h in range(H):
+            s = (Q[b, h] @ K[b, h].T) * scale
+            if causal:
+                s.masked_fill_(mask, float("-inf"))
+            M = s.max(dim=1, keepdim=True).values
+            e = torch.exp(s - M)
+            Pm = e / e.sum(dim=1, keepdim=True)
+            O = rnd(Pm @ V[b, h])
+            D = (dOt[b, h] * O).sum(dim=1, keepdim=True)
+            dS = Pm * (dOt[b, h] @ V[b, h].T - D)
+            dV[b, h] = rnd(rnd(Pm).T @ dOt[b, h])
+            dQ[b, h] = rnd(scale * (rnd(dS) @ K[b, h]))
+            dK[b, h] = rnd(scale * (rnd(dS).T @ Q[b, h]))
+    return dQ.numpy(), dK.numpy(), dV.numpy()

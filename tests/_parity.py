@@ -4,16 +4,18 @@ widening them for the oracle, and the tolerances.
 Tolerances (bf16 inputs/outputs, fp32 accumulation):
   O:        max |err| <= 2e-2 and mean |err| <= 2e-3
   LSE:      max |err| <= 1e-3
-  dQ/dK/dV: |err| <= 5e-2 + 2^-8 |ref| element by element -- the 5e-2 bound
-            plus the rounding of the exact value to the bf16 output format
-            (unit roundoff 2^-8).  On N(0,1) inputs the gradients are O(1)
-            and the second term is negligible; on the peaked-key input they
-            reach ~20, where one bf16 half-ulp alone is 0.0625.
-  Peaked-key backward (a stress input beyond the N(0,1) workloads, where
-  keys c % 64 == 0 are x8): max |err| <= 5e-2 + 3 u max|ref|, u = 2^-8.
-  Three bf16 roundings feed every dQ/dK term there -- dS before the dQ and
-  dK products, the forward's bf16 O inside D = sum dO * O, and the output --
-  and each can reach u relative to the largest terms (|dQ| ~ 19).
+  dQ/dK/dV: max |err| <= 5e-2 on the N(0, 1) forward + backward recipe
+            (assert_grad_max); elsewhere |err| <= 5e-2 + 2^-8 |ref| element
+            by element (assert_grad_close) -- the 5e-2 bound plus the
+            rounding of the exact value to the bf16 output format, which
+            matters where a gradient sums a group of heads (grouped-query
+            K/V) or grows large.
+  Stress inputs whose gradients reach ~20 (the peaked-key input, keys
+  c % 64 == 0 scaled x8): max |err| <= 5e-2 + the error of
+  oracle.bwd_bf16_rounding_model on the same input -- an exact-arithmetic
+  backward whose O, P, dS and outputs are stored in bf16 already misses
+  the exact derivative by that much (0.088 for dQ on heads 0 of the
+  2048-token case, mostly through D = <dO, O> formed from the bf16 O).
 Integer / index results (the ring schedule) must match exactly.
 """
 import numpy as np
@@ -53,11 +55,21 @@ def assert_grad_close(got, ref, what):
     return float(err.max())
 
 
-def assert_grad_close_scaled(got, ref, what):
-    """The peaked-key bound: 5e-2 + 3 u max|ref| (see the module docstring)."""
+def assert_grad_max(got, ref, what):
+    """The gradient bound as stated: max |err| <= 5e-2."""
     err = np.abs(np.asarray(got, dtype=np.float64) - ref)
     assert np.isfinite(err).all(), f"{what}: non-finite values"
-    bound = GRAD_MAX + 3 * BF16_U * float(np.abs(ref).max())
+    mx = float(err.max())
+    assert mx <= GRAD_MAX, f"{what}: max err {mx:.3e}"
+    return mx
+
+
+def assert_grad_close_model(got, ref, model, what):
+    """Stress inputs: max |err| <= 5e-2 + max |model - ref|, where `model` is
+    the bf16-storage rounding model's result (see the module docstring)."""
+    err = np.abs(np.asarray(got, dtype=np.float64) - ref)
+    assert np.isfinite(err).all(), f"{what}: non-finite values"
+    bound = GRAD_MAX + float(np.abs(np.asarray(model) - ref).max())
     mx = float(err.max())
     assert mx <= bound, f"{what}: max err {mx:.3e} > {bound:.3e}"
     return mx

@@ -202,3 +202,12 @@ def test_ulysses_validates_before_any_launch(lib):
     assert call(ws_ptr=FAKE * 5 + 64) == -1             # workspace not 256-byte aligned
     assert call(q=FAKE + 8) == -1
     assert call(P=3) == -1                              # 1024 tokens do not split in 3
+
+
+def test_trace_visits_validates_before_any_cuda_call(lib):
+    # NULL with a capacity, a buffer without one, a negative capacity and a
+    # misaligned buffer are refused before the device is touched
+    assert lib.ring_attn_trace_visits(None, 16) == -1
+    assert lib.ring_attn_trace_visits(ctypes.c_void_p(FAKE), 0) == -1
+    assert lib.ring_attn_trace_visits(ctypes.c_void_p(FAKE), -8) == -1
+    assert lib.ring_attn_trace_visits(ctypes.c_void_p(FAKE + 4), 64) == -1

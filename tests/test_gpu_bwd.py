@@ -1,8 +1,9 @@
 """Backward parity on the GPU against the oracle's plain derivative.
 
 Whole tensors at small shapes (several tiles, ragged chunk tails, causal and
-not, d = 64 and 128).  At the full 128K causal size, in the benchmark's
-launch configuration: sampled dQ rows against the oracle row by row, plus
+not, d = 64 and 128) and at S = 4096.  At the full 128K causal size, in the
+benchmark's launch configuration: sampled dQ, dK and dV rows of two heads
+against the oracle element by element, every LSE row of those heads, plus
 properties that hold at any size (sum_c dV_c = sum_r dO_r, sum_c dK_c = 0).
 """
 import numpy as np
@@ -11,7 +12,7 @@ import torch
 
 import oracle
 import workloads
-from _parity import assert_grad_close, assert_grad_close_scaled, f64
+from _parity import assert_grad_close, assert_grad_close_model, assert_grad_max, assert_lse_close, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -55,19 +56,24 @@ def test_bwd_small_whole_tensor(ra, B, H, S, d, P, causal):
     q, k, v, do, o, lse, dq, dk, dv = _fwd_bwd(ra, inp)
     # the oracle differentiates the exact attention of the same bf16 inputs
     dq_r, dk_r, dv_r, _, _ = oracle.bwd(f64(q), f64(k), f64(v), f64(do), causal, inp["scale"])
-    assert_grad_close(f64(dq), dq_r, "dQ")
-    assert_grad_close(f64(dk), dk_r, "dK")
-    assert_grad_close(f64(dv), dv_r, "dV")
+    assert_grad_max(f64(dq), dq_r, "dQ")
+    assert_grad_max(f64(dk), dk_r, "dK")
+    assert_grad_max(f64(dv), dv_r, "dV")
 
 
 def test_bwd_peaked_keys(ra):
+    # stress input (keys c % 64 == 0 scaled x8, V ~ U(-1, 1)): gradients
+    # reach ~20, and bf16 storage of O, P, dS and the outputs alone misses
+    # the exact derivative by up to ~0.09; the bound adds that model error
     w = workloads.FWD_PEAKED_64K
     inp = workloads.make(w, B=1, H=2, S=2048, P=8, backward=True)
     q, k, v, do, o, lse, dq, dk, dv = _fwd_bwd(ra, inp)
-    dq_r, dk_r, dv_r, _, _ = oracle.bwd(f64(q), f64(k), f64(v), f64(do), False, inp["scale"])
-    assert_grad_close_scaled(f64(dq), dq_r, "dQ")
-    assert_grad_close_scaled(f64(dk), dk_r, "dK")
-    assert_grad_close_scaled(f64(dv), dv_r, "dV")
+    args = (f64(q), f64(k), f64(v), f64(do), False, inp["scale"])
+    dq_r, dk_r, dv_r, _, _ = oracle.bwd(*args)
+    mq, mk, mv = oracle.bwd_bf16_rounding_model(*args)
+    assert_grad_close_model(f64(dq), dq_r, mq, "dQ")
+    assert_grad_close_model(f64(dk), dk_r, mk, "dK")
+    assert_grad_close_model(f64(dv), dv_r, mv, "dV")
 
 
 def test_bwd_repeatable_workspace_reuse(ra):
@@ -83,12 +89,40 @@ def test_bwd_repeatable_workspace_reuse(ra):
         assert (x.float() - y.float()).abs().max().item() <= 1e-2
 
 
+def test_bwd_causal_s4096_whole_tensor(ra):
+    # the 128K fwd+bwd recipe at S = 4096 (P = 4, C = 1024: eight key tiles
+    # per chunk), every element of dQ, dK and dV against the plain derivative
+    inp = workloads.make(workloads.FWDBWD_CAUSAL_128K, B=1, H=2, S=4096, P=4, seed=44)
+    q, k, v, do, o, lse, dq, dk, dv = _fwd_bwd(ra, inp)
+    dq_r, dk_r, dv_r, _, _ = oracle.bwd(f64(q), f64(k), f64(v), f64(do), True, inp["scale"])
+    assert_grad_max(f64(dq), dq_r, "dQ")
+    assert_grad_max(f64(dk), dk_r, "dK")
+    assert_grad_max(f64(dv), dv_r, "dV")
+
+
 @pytest.mark.slow
-def test_bwd_causal_128k_sampled_and_properties(ra):
+def test_bwd_causal_128k_sampled_rows(ra):
+    # The full fwd+bwd workload (B=1, H=32, S=131072, d=128, P=4, causal), in
+    # the benchmark's launch configuration.  For heads 0 and H-1, at sampled
+    # positions (0, S-1, the first and last rows of every chunk and their
+    # neighbours, 48 seeded random ones), element by element:
+    #   dQ rows      -- oracle.bwd_dq_rows (LSE_r and D_r per sampled row);
+    #   dK, dV rows  -- oracle.bwd_dkdv_rows, which takes LSE_r and D_r of
+    #                   every query row r >= c of the head from the definition;
+    #   LSE          -- every row of the head, from the same pass.
     w = workloads.FWDBWD_CAUSAL_128K
     inp = workloads.make(w, keep_fp32=False)
     q, k, v, do, o, lse, dq, dk, dv = _fwd_bwd(ra, inp)
-    H, S, d, P = inp["H"], inp["S"], inp["d"], inp["P"]
+    H, S, d, P, sc = inp["H"], inp["S"], inp["d"], inp["P"], inp["scale"]
+    local = workloads.sample_rows(1, 1, S, P, n_random=48).numpy()
+    for bh in (0, H - 1):
+        qh, kh, vh, dh = (f64(x[0:1, bh:bh + 1]) for x in (q, k, v, do))
+        dq_r, _ = oracle.bwd_dq_rows(qh, kh, vh, dh, True, sc, local)
+        assert_grad_max(f64(dq[0, bh])[local], dq_r, f"dQ head {bh}")
+        dk_r, dv_r, lse_r, _ = oracle.bwd_dkdv_rows(qh, kh, vh, dh, True, sc, local, block=512)
+        assert_grad_max(f64(dk[0, bh])[local], dk_r, f"dK head {bh}")
+        assert_grad_max(f64(dv[0, bh])[local], dv_r, f"dV head {bh}")
+        assert_lse_close(f64(lse[0, bh]), lse_r, f"LSE head {bh}")
     # properties over every head: rows of P sum to 1 and sum_c dS_rc = 0
     dv_sum = dv.float().sum(dim=2)
     do_sum = do.float().sum(dim=2)
@@ -96,11 +130,5 @@ def test_bwd_causal_128k_sampled_and_properties(ra):
     scale_ref = do.float().abs().sum(dim=2).max().item()
     assert (dv_sum - do_sum).abs().max().item() <= 1e-2 * scale_ref
     assert dk_sum.abs().max().item() <= 1e-2 * scale_ref
-    # sampled dQ rows of two heads against the oracle
-    local = workloads.sample_rows(1, 1, S, P, n_random=48).numpy()
-    for bh in (0, H - 1):
-        qh, kh, vh, dh = (f64(x[0:1, bh:bh + 1]) for x in (q, k, v, do))
-        dq_r, _ = oracle.bwd_dq_rows(qh, kh, vh, dh, True, inp["scale"], local)
-        assert_grad_close(f64(dq[0, bh])[local], dq_r, f"dQ head {bh}")
     for t in (dq, dk, dv):
         assert torch.isfinite(t.float()).all()

@@ -3,9 +3,10 @@ fp64 oracle on identical seeded bf16 inputs.
 
 Small shapes are compared element by element over whole tensors (several
 tiles per chunk, ragged chunk tails, P = 1, causal and not, d = 64 and 128).
-The full-size workloads run in the same launch configuration the benchmark
-times and are compared on sampled rows (row 0, first/last rows of every
-chunk and their neighbours, 256 seeded random rows) of a few heads.
+The 32K causal workload is compared over every element of every head; the
+larger workloads run in the same launch configuration the benchmark times
+and are compared on sampled rows (row 0, first/last rows of every chunk and
+their neighbours, seeded random rows) of a few heads.
 """
 import math
 
@@ -142,9 +143,17 @@ def _sampled(ra, w, heads, n_random=192):
 
 
 @pytest.mark.slow
-def test_fwd_causal_32k_sampled(ra):
+def test_fwd_causal_32k_whole_tensor(ra):
+    # B=1, H=32, S=32768, d=128, P=4, causal: every element of O and LSE of
+    # every head against the definition (row blocks, fp64, one head at a time)
     w = workloads.FWD_CAUSAL_32K
-    _sampled(ra, w, heads=[0, 13, w.B * w.H - 1])
+    inp = workloads.make(w, keep_fp32=False)
+    q, k, v, o, lse = _run(ra, inp)
+    for h in range(w.H):
+        qh, kh, vh = (f64(x[0:1, h:h + 1]) for x in (q, k, v))
+        o_ref, lse_ref = oracle.naive_fwd_blocked(qh, kh, vh, True, inp["scale"], block=512)
+        assert_o_close(f64(o[0:1, h:h + 1]), o_ref, f"O head {h}")
+        assert_lse_close(f64(lse[0:1, h:h + 1]), lse_ref, f"LSE head {h}")
 
 
 @pytest.mark.slow

@@ -18,6 +18,15 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 rng = np.random.default_rng(20240601)
 
 
+# Both whole-tensor forward routines answer to the same pins: the C loops and
+# the row-block PyTorch pass (blocks of 3 rows here, so every case spans
+# several blocks).
+FWD_IMPLS = {
+    "c_loops": oracle.naive_fwd,
+    "row_blocks": lambda q, k, v, causal, scale: oracle.naive_fwd_blocked(q, k, v, causal, scale, block=3),
+}
+
+
 def _rand(B, H, S, d, seed):
     g = np.random.default_rng(seed)
     return (g.standard_normal((B, H, S, d)), g.standard_normal((B, H, S, d)),
@@ -28,38 +37,41 @@ def _rand(B, H, S, d, seed):
 # naive_fwd: textbook special cases
 # --------------------------------------------------------------------------
 
+@pytest.mark.parametrize("impl", FWD_IMPLS)
 @pytest.mark.parametrize("causal", [False, True])
-def test_single_key_returns_that_value(causal):
+def test_single_key_returns_that_value(causal, impl):
     # S = 1: the only key gets weight 1, so O = v_0 and LSE = s_00.
     q = np.array([[[[0.5, -1.0, 2.0]]]])
     k = np.array([[[[1.5, 0.25, -0.5]]]])
     v = np.array([[[[3.0, -7.0, 0.125]]]])
-    o, lse = oracle.naive_fwd(q, k, v, causal, 0.7)
+    o, lse = FWD_IMPLS[impl](q, k, v, causal, 0.7)
     s00 = 0.7 * (0.5 * 1.5 - 1.0 * 0.25 + 2.0 * -0.5)
     assert np.array_equal(o[0, 0, 0], v[0, 0, 0])
     assert lse[0, 0, 0] == pytest.approx(s00, abs=1e-15)
 
 
-def test_hand_computed_d1():
+@pytest.mark.parametrize("impl", FWD_IMPLS)
+def test_hand_computed_d1(impl):
     # d = 1, scale = 1, q = 1, keys 0 and ln 3 -> scores 0, ln 3,
     # weights 1/4 and 3/4; values 2 and 6 -> O = 0.5 + 4.5 = 5; LSE = ln 4.
     q = np.array([[[[1.0], [1.0]]]])
     k = np.array([[[[0.0], [math.log(3.0)]]]])
     v = np.array([[[[2.0], [6.0]]]])
-    o, lse = oracle.naive_fwd(q, k, v, False, 1.0)
+    o, lse = FWD_IMPLS[impl](q, k, v, False, 1.0)
     assert o[0, 0, 1, 0] == pytest.approx(5.0, abs=1e-14)
     assert lse[0, 0, 1] == pytest.approx(math.log(4.0), abs=1e-15)
     # causal: row 0 sees only key 0 -> O = 2, LSE = 0; row 1 as above.
-    o, lse = oracle.naive_fwd(q, k, v, True, 1.0)
+    o, lse = FWD_IMPLS[impl](q, k, v, True, 1.0)
     assert o[0, 0, 0, 0] == 2.0 and lse[0, 0, 0] == 0.0
     assert o[0, 0, 1, 0] == pytest.approx(5.0, abs=1e-14)
 
 
-def test_two_keys_sigmoid_weights():
+@pytest.mark.parametrize("impl", FWD_IMPLS)
+def test_two_keys_sigmoid_weights(impl):
     # Two keys: weight of key 0 is the logistic function of s_0 - s_1.
     q, k, v = _rand(1, 1, 2, 5, 1)
     scale = 0.37
-    o, lse = oracle.naive_fwd(q, k, v, False, scale)
+    o, lse = FWD_IMPLS[impl](q, k, v, False, scale)
     for r in range(2):
         s0 = scale * float(q[0, 0, r] @ k[0, 0, 0])
         s1 = scale * float(q[0, 0, r] @ k[0, 0, 1])
@@ -70,14 +82,15 @@ def test_two_keys_sigmoid_weights():
                                              abs=1e-14)
 
 
+@pytest.mark.parametrize("impl", FWD_IMPLS)
 @pytest.mark.parametrize("causal", [False, True])
-def test_rows_sum_to_one_and_match_high_precision(causal):
+def test_rows_sum_to_one_and_match_high_precision(causal, impl):
     # With S == d and V = I, O_r is the attention row P_r itself.
     S = d = 8
     q, k, _ = _rand(1, 1, S, d, 2)
     v = np.eye(S)[None, None]
     scale = 1.0 / math.sqrt(d)
-    o, lse = oracle.naive_fwd(q, k, v, causal, scale)
+    o, lse = FWD_IMPLS[impl](q, k, v, causal, scale)
     np.testing.assert_allclose(o.sum(-1), 1.0, rtol=0, atol=1e-12)
     mpmath.mp.dps = 40
     for r in range(S):
@@ -91,27 +104,30 @@ def test_rows_sum_to_one_and_match_high_precision(causal):
             assert o[0, 0, r, c] == pytest.approx(p, abs=1e-14)
 
 
+@pytest.mark.parametrize("impl", FWD_IMPLS)
 @pytest.mark.parametrize("causal", [False, True])
-def test_constant_v_gives_constant_o(causal):
+def test_constant_v_gives_constant_o(causal, impl):
     q, k, _ = _rand(2, 3, 17, 6, 3)
     v = np.broadcast_to(np.array([1.5, -2.0, 0.25, 3.0, -0.75, 9.0]), q.shape).copy()
-    o, _ = oracle.naive_fwd(q, k, v, causal, 0.9)
+    o, _ = FWD_IMPLS[impl](q, k, v, causal, 0.9)
     np.testing.assert_allclose(o, v, rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("impl", FWD_IMPLS)
 @pytest.mark.parametrize("causal", [False, True])
-def test_zero_q_is_uniform_average(causal):
+def test_zero_q_is_uniform_average(causal, impl):
     B, H, S, d = 1, 2, 9, 4
     _, k, v = _rand(B, H, S, d, 4)
     q = np.zeros((B, H, S, d))
-    o, lse = oracle.naive_fwd(q, k, v, causal, 0.5)
+    o, lse = FWD_IMPLS[impl](q, k, v, causal, 0.5)
     for r in range(S):
         n = r + 1 if causal else S
         np.testing.assert_allclose(o[:, :, r], v[:, :, :n].mean(axis=2), rtol=0, atol=1e-13)
         np.testing.assert_allclose(lse[:, :, r], math.log(n), rtol=0, atol=1e-14)
 
 
-def test_brute_force_high_precision_random():
+@pytest.mark.parametrize("impl", FWD_IMPLS)
+def test_brute_force_high_precision_random(impl):
     # Independent 40-digit evaluation of the definition on tiny random inputs.
     B, H, S, d = 1, 2, 6, 3
     q, k, v = _rand(B, H, S, d, 5)
@@ -119,7 +135,7 @@ def test_brute_force_high_precision_random():
     scale = 0.8
     mpmath.mp.dps = 40
     for causal in (False, True):
-        o, lse = oracle.naive_fwd(q, k, v, causal, scale)
+        o, lse = FWD_IMPLS[impl](q, k, v, causal, scale)
         for h in range(H):
             for r in range(S):
                 allowed = range(r + 1) if causal else range(S)
@@ -142,12 +158,13 @@ def test_rows_api_matches_whole_rows():
     np.testing.assert_array_equal(lse_r, lse.reshape(-1)[rows])
 
 
-def test_large_scores_do_not_overflow():
+@pytest.mark.parametrize("impl", FWD_IMPLS)
+def test_large_scores_do_not_overflow(impl):
     # Max subtraction: scores near 1000 must not overflow exp.
     q = np.full((1, 1, 3, 1), 40.0)
     k = np.array([[[[25.0], [24.0], [-5.0]]]])
     v = np.array([[[[1.0], [2.0], [3.0]]]])
-    o, lse = oracle.naive_fwd(q, k, v, False, 1.0)
+    o, lse = FWD_IMPLS[impl](q, k, v, False, 1.0)
     w = np.exp(np.array([1000.0, 960.0, -200.0]) - 1000.0)
     w /= w.sum()
     np.testing.assert_allclose(o[0, 0, 0, 0], w @ np.array([1.0, 2.0, 3.0]), atol=1e-15)
@@ -331,6 +348,97 @@ def test_backward_dq_rows_matches_full():
     dq_r, D_r = oracle.bwd_dq_rows(q, k, v, dO, True, 0.6, rows)
     np.testing.assert_allclose(dq_r, dq.reshape(-1, 5)[rows], atol=1e-13)
     np.testing.assert_allclose(D_r, D.reshape(-1)[rows], atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_key_rows_finite_differences(causal):
+    # dK_c and dV_c of chosen key rows, with LSE and D taken over every query
+    # row inside the routine, against central differences of L = sum(dO * O)
+    # in the key row's own entries.
+    S, d = 7, 3
+    q, k, v = _rand(1, 1, S, d, 61)
+    dO = np.random.default_rng(62).standard_normal(q.shape)
+    scale = 0.8
+    keys = np.array([0, 3, 6])
+    dk, dv, lse, D = oracle.bwd_dkdv_rows(q, k, v, dO, causal, scale, keys, block=2)
+    eps = 1e-6
+    for n, c in enumerate(keys):
+        for x in range(d):
+            for name, grad in (("k", dk), ("v", dv)):
+                a = {"q": q, "k": k.copy(), "v": v.copy()}
+                b = {"q": q, "k": k.copy(), "v": v.copy()}
+                a[name][0, 0, c, x] += eps
+                b[name][0, 0, c, x] -= eps
+                num = (_loss(a["q"], a["k"], a["v"], dO, causal, scale)
+                       - _loss(b["q"], b["k"], b["v"], dO, causal, scale)) / (2 * eps)
+                assert abs(num - grad[n, x]) <= 1e-6 * max(1.0, abs(num)), (name, c, x)
+    # D_r = sum_k dO_rk O_rk (the identity sum_c P_rc dP_rc = <dO_r, O_r>)
+    o, lse_ref = oracle.naive_fwd(q, k, v, causal, scale)
+    np.testing.assert_allclose(D, (dO * o).sum(-1)[0, 0], atol=1e-13)
+    np.testing.assert_allclose(lse, lse_ref[0, 0], atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_key_rows_match_full(causal):
+    # Many row blocks, keys on and off the block edges, against the C loops.
+    S, d = 200, 8
+    q, k, v = _rand(1, 1, S, d, 71)
+    dO = np.random.default_rng(72).standard_normal(q.shape)
+    dq, dk, dv, lse, D = oracle.bwd(q, k, v, dO, causal, 0.45)
+    keys = np.array([0, 1, 31, 32, 33, 100, 150, 198, 199])
+    dk_r, dv_r, lse_r, D_r = oracle.bwd_dkdv_rows(q, k, v, dO, causal, 0.45, keys, block=32)
+    np.testing.assert_allclose(dk_r, dk[0, 0][keys], atol=1e-13)
+    np.testing.assert_allclose(dv_r, dv[0, 0][keys], atol=1e-13)
+    np.testing.assert_allclose(lse_r, lse[0, 0], atol=1e-13)
+    np.testing.assert_allclose(D_r, D[0, 0], atol=1e-13)
+    # every key: the column sums sum_c dV_c = sum_r dO_r and sum_c dK_c = 0
+    dk_a, dv_a, _, _ = oracle.bwd_dkdv_rows(q, k, v, dO, causal, 0.45, np.arange(S), block=32)
+    np.testing.assert_allclose(dv_a.sum(0), dO[0, 0].sum(0), atol=1e-12)
+    np.testing.assert_allclose(dk_a.sum(0), 0, atol=1e-12)
+
+
+def test_backward_key_rows_rejects_bad_input():
+    q, k, v = _rand(1, 2, 8, 4, 73)
+    with pytest.raises(ValueError):
+        oracle.bwd_dkdv_rows(q, k, v, q, True, 0.5, [0])          # two heads
+    with pytest.raises(ValueError):
+        oracle.bwd_dkdv_rows(q[:, :1], k[:, :1], v[:, :1], q[:, :1], True, 0.5, [8])
+
+
+def test_bf16_rounding_matches_the_library_conversion():
+    # the rounding model's bf16 step against torch's own fp32 -> bf16
+    # conversion (round to nearest even), including exact ties
+    import torch
+    from oracle.oracle import _bf16_rne
+    g = torch.Generator().manual_seed(81)
+    x = torch.randn(200000, generator=g, dtype=torch.float64) * torch.exp(
+        torch.randn(200000, generator=g, dtype=torch.float64) * 8)
+    ties = torch.tensor([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 2 ** -130, 0.0, -0.0,
+                         float("inf"), -float("inf")], dtype=torch.float64)
+    for t in (x, ties):
+        want = t.to(torch.float32).to(torch.bfloat16).to(torch.float64)
+        assert torch.equal(_bf16_rne(t), want)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_rounding_model_without_rounding_is_the_derivative(causal):
+    # every rounding replaced by the identity leaves the plain derivative,
+    # which the finite-difference pins above fix
+    q, k, v = _rand(2, 2, 24, 8, 91)
+    dO = np.random.default_rng(92).standard_normal(q.shape)
+    dq, dk, dv, _, _ = oracle.bwd(q, k, v, dO, causal, 0.35)
+    mq, mk, mv = oracle.bwd_bf16_rounding_model(q, k, v, dO, causal, 0.35, round_bf16=False)
+    np.testing.assert_allclose(mq, dq, atol=1e-12)
+    np.testing.assert_allclose(mk, dk, atol=1e-12)
+    np.testing.assert_allclose(mv, dv, atol=1e-12)
+    # with rounding, every output is a bf16 value and lies within a few bf16
+    # units of the exact derivative on N(0, 1) inputs
+    import torch
+    rq, rk, rv = oracle.bwd_bf16_rounding_model(q, k, v, dO, causal, 0.35)
+    for got, ref in ((rq, dq), (rk, dk), (rv, dv)):
+        t = torch.as_tensor(got)
+        assert torch.equal(t, t.to(torch.float32).to(torch.bfloat16).to(torch.float64))
+        assert np.abs(got - ref).max() <= 4 * 2.0 ** -8 * max(1.0, np.abs(ref).max())
 
 
 # --------------------------------------------------------------------------
