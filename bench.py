@@ -45,18 +45,23 @@ import workloads  # noqa: E402
 
 METRIC = "attention TFLOP/s and tokens/s at 1 GB300 (fwd, fwd+bwd); % of dense BF16 peak"
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch at the
-# 128K forward + backward shape, from one ncu capture (the command is in
-# profiles/launches_fwdbwd_causal_h32_s131072_d128_p4.md).  Each entry is
-# tied to a hash of the kernel's source; once the source changes the figure
-# no longer describes the kernel and the line reports traffic as null.
-KERNEL_TRAFFIC = {
-    "ring_fwd_kernel": {"bytes": 3440709888 + 1156451072,
-                        "sources": ("fwd_kernel.cuh", "sm103_ptx.cuh", "layout.cuh"),
-                        "sha1": "3668f7caca854fcf9c730712a7af52dfea77dd67"},
-    "ring_bwd_kernel": {"bytes": 14108758784 + 8614416640,
-                        "sources": ("bwd_kernel.cuh", "sm103_ptx.cuh", "layout.cuh"),
-                        "sha1": "cd65027825d2c5ccc3080088bf0ee7a7a85fc0ce"},
+# Hardware counters of the main kernels from ncu captures, per launch of
+# the 128K forward + backward workload (B=1, H=32, S=131072, d=128, P=4,
+# causal).  The DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum)
+# come from a capture of the same shape with 4 heads instead of 32 -- each
+# head's CTAs run apart from the others', so the bytes grow with the heads
+# -- scaled by 32 / 4; the tensor-pipe share
+# (sm__pipe_tensor_cycles_active, % of elapsed cycles) from a full-set
+# capture of the same kernel.  Each entry is tied to a hash of the kernel's
+# source: once the source changes the counters no longer describe the
+# kernel and the line reports them as null.
+KERNEL_COUNTERS = {
+    "ring_fwd_kernel": {"traffic": None, "tensor_pipe_pct": None,
+                        "sources": ("fwd_kernel.cuh", "sm103_ptx.cuh", "layout.cuh", "trace.cuh"),
+                        "sha1": None},
+    "ring_bwd_kernel": {"traffic": None, "tensor_pipe_pct": None,
+                        "sources": ("bwd_kernel.cuh", "sm103_ptx.cuh", "layout.cuh", "trace.cuh"),
+                        "sha1": None},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -91,21 +96,27 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def recorded_traffic(kernel: str, workload: str, S: int, H: int):
-    """Bytes per launch from the recorded capture, or None if the kernel's
-    source changed since, or the shape is not the captured one."""
+def source_sha1(files) -> str:
     import hashlib
-    rec = KERNEL_TRAFFIC.get(kernel)
-    if rec is None or workload != workloads.FWDBWD_CAUSAL_128K.name:
-        return None
-    if S != workloads.FWDBWD_CAUSAL_128K.S or H != workloads.FWDBWD_CAUSAL_128K.H:
-        return None
     m = hashlib.sha1()
     csrc = os.path.join(ROOT, "long_context_exact_ring_gb300", "csrc")
-    for f in rec["sources"]:
+    for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:
             m.update(fh.read())
-    return rec["bytes"] if m.hexdigest() == rec["sha1"] else None
+    return m.hexdigest()
+
+
+def recorded_counters(kernel: str, workload: str, S: int, H: int):
+    """(traffic bytes per launch, tensor-pipe %) from the recorded captures,
+    each None if the kernel's source changed since or the shape is not the
+    captured one."""
+    rec = KERNEL_COUNTERS.get(kernel)
+    w = workloads.FWDBWD_CAUSAL_128K
+    if rec is None or rec["sha1"] is None or workload != w.name or S != w.S or H != w.H:
+        return None, None
+    if source_sha1(rec["sources"]) != rec["sha1"]:
+        return None, None
+    return rec["traffic"], rec["tensor_pipe_pct"]
 
 
 def pair_count(S: int, causal: bool) -> int:
@@ -353,11 +364,39 @@ def main():
     dom_ms = prof[dom][1] / max(1, prof[dom][0])
     dom_flop = f_fwd if dom == "ring_fwd_kernel" else f_bwd
     achieved = dom_flop / (dom_ms / 1e3) / 1e12
+    dom_traffic, dom_tensor = recorded_counters(dom, w.name, S, H)
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_sus,
                 "unit": "TFLOP/s", "frac": achieved / peak_sus,
-                "traffic": recorded_traffic(dom, w.name, S, H),
+                "traffic": dom_traffic,
                 "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a multi-second step)",
                 "frac_of_burst_peak": achieved / peak_burst}
+    for name, pas in (("ring_fwd_kernel", "fwd"), ("ring_bwd_kernel", "bwd_main")):
+        if pas in passes:
+            traffic, tensor_pct = recorded_counters(name, w.name, S, H)
+            passes[pas]["ncu_tensor_pipe_pct"] = tensor_pct
+            passes[pas]["ncu_dram_bytes"] = traffic
+
+    # ---- memory-bound kernels against the measured HBM peak -----------------
+    # algorithmic bytes per launch: bwd_prep reads O and dO (bf16) and LSE,
+    # writes D and LSE2 (fp32); dq_convert reads the fp32 accumulator and
+    # writes bf16 dQ; merge (timed below, in the emulated ring) reads two fp32
+    # partials and their LSE and writes one of each.
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    rows = B * H * S
+    mem_bytes = {"bwd_prep_kernel": rows * (2 * d * 2 + 4 + 8),
+                 "dq_convert_kernel": rows * d * (4 + 2),
+                 "merge_partials_kernel": rows * (3 * d * 4 + 3 * 4)}
+
+    def hbm_entry(name, n, ms_total):
+        if not n:
+            return None
+        avg = ms_total / n
+        gbs = mem_bytes[name] / (avg / 1e3) / 1e9
+        return {"launches": n, "ms": avg, "bytes": mem_bytes[name], "gbs": gbs,
+                "frac_of_hbm": gbs / hbm_peak, "hbm_peak_gbs": hbm_peak,
+                "peak_source": f"{peak_src} copy bandwidth"}
+    memory_kernels = {n: hbm_entry(n, *prof[n]) for n in ("bwd_prep_kernel", "dq_convert_kernel")
+                      if prof[n][0]}
 
     # ---- end to end through the public API with host buffers ---------------
     # Every step copies its inputs from pinned host memory and reads its
@@ -454,8 +493,16 @@ def main():
         o_e = torch.empty_like(q)
         lse_e = torch.empty_like(lse)
         fused = timed(lambda: ra.ring_attn_fwd(q, k, v, P, causal, sc, o=o, lse=lse, stream=stream))
+        # the emulated ring's per-step merges run at the workload's full size
+        # ([B, H, S, d] fp32 partials): time them with the library's events
+        ra.profile_enable(True)
+        ra.profile_reset()
         over = timed(lambda: ra.ring_attn_fwd_emulated(q, k, v, P, causal, sc, overlap=True, o=o_e,
                                                        lse=lse_e, workspace=ws_e, stream=stream))
+        mprof = ra.profile_read()
+        ra.profile_enable(False)
+        memory_kernels["merge_partials_kernel"] = hbm_entry("merge_partials_kernel",
+                                                            *mprof["merge_partials_kernel"])
         serial = timed(lambda: ra.ring_attn_fwd_emulated(q, k, v, P, causal, sc, overlap=False, o=o_e,
                                                          lse=lse_e, workspace=ws_e, stream=stream))
         if ra.check_status() != ra.RA_OK:
@@ -508,6 +555,7 @@ def main():
             "tokens_per_s": tokens,
             "passes": passes,
             "roofline": roofline,
+            "memory_kernels": memory_kernels,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "ring_emulation": emu,

@@ -288,7 +288,7 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             for (int n = 0; n < NT; ++n, qi.next()) {
                 const int s = n % CF::kStages;
                 const uint32_t ph = (uint32_t)(n / CF::kStages) & 1u;
-                ok = mbar_wait(bar_qdo_empty(s), ph ^ 1u, wc);
+                ok = mbar_wait_poll(bar_qdo_empty(s), ph ^ 1u, wc);
                 if (!ok) break;
                 const int q0 = qi.q_start();
                 const int qh = qi.q_head();
@@ -436,12 +436,12 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 const int s = n % CF::kStages;
                 const uint32_t par = (uint32_t)n & 1u;
                 const int q0 = qi.q_start();
-                if (!mbar_wait(bar_dqa_staged, par, wc)) break;
+                if (!mbar_wait_poll(bar_dqa_staged, par, wc)) break;
 #pragma unroll
                 for (int b = 0; b < D / 32; ++b)
                     tma_reduce_add_3d(&map_dq, sDS + (uint32_t)b * 8192u, 32 * b, q0, qi.q_head());
                 bulk_commit_group();
-                if (!mbar_wait(bar_dqb_staged, par, wc)) break;
+                if (!mbar_wait_poll(bar_dqb_staged, par, wc)) break;
 #pragma unroll
                 for (int b = 0; b < D / 32; ++b)
                     tma_reduce_add_3d(&map_dq, sDO + s * CF::kTileBytes + (uint32_t)b * 8192u, 32 * b, q0 + 64,
@@ -450,7 +450,7 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 bulk_wait_read_1();
                 mbar_arrive(bar_ds_free);
                 bulk_wait_read_all();
-                if (!mbar_wait(bar_k_done(s), (uint32_t)(n / CF::kStages) & 1u, wc)) break;   // dK read Q
+                if (!mbar_wait_poll(bar_k_done(s), (uint32_t)(n / CF::kStages) & 1u, wc)) break;   // dK read Q
                 mbar_arrive(bar_qdo_empty(s));
             }
             bulk_wait_all();

@@ -133,6 +133,46 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
     return mbar_wait_slow(bar, parity, w);
 }
 
+// Non-blocking test of a phase.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0u;
+}
+
+// Wait by polling: for a lone thread on a hand-off loop (the TMA producer,
+// the dQ reducer), where a suspended thread's wake-up is on the critical
+// path.  The clock is read every 64 polls; the same limit and abort flag
+// as mbar_wait bound it.
+__device__ __noinline__ bool mbar_wait_poll_slow(uint32_t bar, uint32_t parity, const WaitCtl& w)
+{
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (mbar_test_wait(bar, parity)) return true;
+        if (*w.abort_flag) return false;
+        if (globaltimer_ns() - t0 > w.limit_ns) {
+            *w.abort_flag = 1;
+            atomicOr(w.status, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity, const WaitCtl& w)
+{
+    if (mbar_test_wait(bar, parity)) return true;
+    return mbar_wait_poll_slow(bar, parity, w);
+}
+
 // ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor) loads into shared memory, completing on an
 // mbarrier with a transaction count.
