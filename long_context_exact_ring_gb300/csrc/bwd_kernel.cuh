@@ -34,11 +34,15 @@
 // TMEM while dK runs (warp of lane quarter q, warpgroup g: queries
 // 32q..32q+31, d columns [g D/4, (g+1) D/4)) and release the region.  They
 // write the scaled fp32 tile at once as 128-byte swizzled boxes of 32
-// columns x 64 rows: rows 0-63 into the dS buffer (the dQ MMA has read it),
-// rows 64-127 into the tile's dO buffer (dV has read it).  One thread adds
+// columns x 64 rows.  At D = 128, dS itself was written into the tile's dO
+// buffer once dV had read it; rows 0-63 of dQ go there after the dQ MMA has
+// read dS, rows 64-127 into a staging buffer of their own.  One thread adds
 // both halves to the fp32 dQ accumulator in global memory with TMA bulk
-// reduce-adds, frees the dS buffer, and hands the stage back to the
-// producer once dK has read its Q as well.
+// reduce-adds (the SM drains reductions at ~25 B/clk, so 64 KB take some
+// 2,600+ cycles), hands the stage back to the producer as soon as the
+// first half has been read and dK has read Q, and frees the staging buffer
+// after the second.  (At D = 64 dO is too small for dS: dS keeps a buffer
+// of its own and both dQ halves go to the staging buffer.)
 //
 // CTA layout (640 threads, five warpgroups):
 //   WG0    warp 0 TMA producer (K, V once; Q, dO, LSE2, D tiles in ring
@@ -74,12 +78,20 @@ struct Cfg {
     static constexpr int kTileBytes = 128 * D * 2;
     static constexpr int kStages = 2;                       // Q / dO / row stages
     static constexpr int kRowBytes = kBQ * 4;               // one LSE2 or D row tile
+    // D = 128: dS (128 x 128 bf16, as large as a dO tile) is written into the
+    // tile's dO buffer once dV has read it, so the 32 KB a separate dS buffer
+    // would take hold the dQ staging of rows 64-127 instead.  D = 64: dO is
+    // half that size, so dS keeps its own buffer and the staging buffer
+    // holds the whole dQ tile (128 rows x 64 columns fp32).
+    static constexpr bool kDsInDo = (D == 128);
+    static constexpr int kStgBytes = 32768;
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kOffK + kTileBytes;
     static constexpr int kOffQ = kOffV + kTileBytes;
     static constexpr int kOffDO = kOffQ + kStages * kTileBytes;
-    static constexpr int kOffDS = kOffDO + kStages * kTileBytes;        // 128 x 128 bf16
-    static constexpr int kOffRow = kOffDS + 2 * kBoxBytes;              // [stage][lse2 | D]
+    static constexpr int kOffStg = kOffDO + kStages * kTileBytes;       // dQ staging
+    static constexpr int kOffDS = kOffStg + kStgBytes;                  // dS (D = 64 only)
+    static constexpr int kOffRow = kOffDS + (kDsInDo ? 0 : 2 * kBoxBytes);   // [stage][lse2 | D]
     static constexpr int kOffBar = kOffRow + kStages * 2 * kRowBytes;
     static constexpr int kBarBytes = 256;
     static constexpr int kSmemBytes = kOffBar + kBarBytes;
@@ -173,12 +185,21 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     const uint32_t sV = base + CF::kOffV;
     const uint32_t sQ = base + CF::kOffQ;
     const uint32_t sDO = base + CF::kOffDO;
-    const uint32_t sDS = base + CF::kOffDS;
+    const uint32_t sStg = base + CF::kOffStg;
+    // dS of a tile in stage s: the stage's dO buffer, or the dS buffer
+    auto ds_off = [&](int s) { return CF::kDsInDo ? CF::kOffDO + s * CF::kTileBytes : CF::kOffDS; };
     const uint32_t sRow = base + CF::kOffRow;
     const uint32_t bar0 = base + CF::kOffBar;
     const uint32_t bar_kv = bar0;
-    auto bar_qdo_full = [&](int s) { return bar0 + 8u * (1 + s); };
-    auto bar_qdo_empty = [&](int s) { return bar0 + 8u * (3 + s); };
+    // Q (with the LSE2 rows) and dO (with the D rows) of a stage arrive and
+    // are released separately: Q is free once dK has read it (k_done), dO
+    // once the tile is past its dS phase and, at D = 128, the dQ rows staged
+    // there after dS have been reduced (do_empty, from the reducer).  The next tile's S^T can then start
+    // while its dO is still loading behind the reductions that share the
+    // SM's memory port.
+    auto bar_q_full = [&](int s) { return bar0 + 8u * (1 + s); };
+    auto bar_do_full = [&](int s) { return bar0 + 8u * (3 + s); };
+    auto bar_do_empty = [&](int s) { return bar0 + 8u * (19 + s); };
     const uint32_t bar_s_full = bar0 + 8u * 5;
     const uint32_t bar_dp_full = bar0 + 8u * 6;
     const uint32_t bar_p_ready = bar0 + 8u * 7;
@@ -191,14 +212,16 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     // the MMA can finish the next tile's dK before the reducer frees this
     // stage, but not the tile after (it needs this stage back).
     auto bar_k_done = [&](int s) { return bar0 + 8u * (s == 0 ? 13u : 17u); };
-    // The dQ tile is staged in two halves: rows 0-63 in the dS buffer (free
-    // once the dQ MMA has read it), rows 64-127 in the tile's dO buffer
-    // (free once dV has read it; dV is issued before dQ).  Neither waits for
-    // dK; the stage is handed back once dK has read Q and the dO half has
-    // been reduced.
-    const uint32_t bar_dqa_staged = bar0 + 8u * 14;  // rows 0-63 sit in the dS buffer
-    const uint32_t bar_dqb_staged = bar0 + 8u * 15;  // rows 64-127 sit in the dO buffer
-    const uint32_t bar_ds_free = bar0 + 8u * 16;     // the dS buffer's half has been read
+    // The dQ tile is staged in two halves.  D = 128: rows 0-63 in the tile's
+    // dO buffer, where dS was (free once the dQ MMA has read it), rows 64-127
+    // in the staging buffer; the stage is handed back once dK has read Q and
+    // the first half has been reduced.  D = 64: both halves in the staging
+    // buffer; the stage is handed back once dK has read Q.
+    const uint32_t bar_dqa_staged = bar0 + 8u * 14;  // rows 0-63 staged
+    const uint32_t bar_dqb_staged = bar0 + 8u * 15;  // rows 64-127 staged
+    const uint32_t bar_stg_free = bar0 + 8u * 16;    // the staging buffer's rows have been read
+    // dV of the stage's tile has read its dO (D = 128: dS may go there).
+    auto bar_dv_done = [&](int s) { return bar0 + 8u * (s == 0 ? 18u : 21u); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + CF::kOffBar + 192);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + CF::kOffBar + 200);
 
@@ -225,8 +248,10 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         *abort_flag = 0;
         mbar_init(bar_kv, 1);
         for (int s = 0; s < CF::kStages; ++s) {
-            mbar_init(bar_qdo_full(s), 1);
-            mbar_init(bar_qdo_empty(s), 1);
+            mbar_init(bar_q_full(s), 1);
+            mbar_init(bar_do_full(s), 1);
+            mbar_init(bar_do_empty(s), 1);
+            mbar_init(bar_dv_done(s), 1);
         }
         mbar_init(bar_s_full, 1);
         mbar_init(bar_dp_full, 1);
@@ -239,7 +264,7 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         for (int s = 0; s < CF::kStages; ++s) mbar_init(bar_k_done(s), 1);
         mbar_init(bar_dqa_staged, kSoftmaxThreads / 2);
         mbar_init(bar_dqb_staged, kSoftmaxThreads / 2);
-        mbar_init(bar_ds_free, 1);
+        mbar_init(bar_stg_free, 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -279,16 +304,16 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                     tma_load_3d(sV + x * CF::kBoxBytes, &map_v, bar_kv, 64 * x, k0, bkv);
                 }
             }
-            int issued[CF::kStages];
-            for (int s = 0; s < CF::kStages; ++s) issued[s] = -1;
+            int issued_q[CF::kStages], issued_do[CF::kStages];
+            for (int s = 0; s < CF::kStages; ++s) issued_q[s] = issued_do[s] = -1;
             bool ok = true;
-            constexpr uint32_t kStageTx = 2 * CF::kTileBytes + (kRowTma ? 2 * CF::kRowBytes : 0);
+            constexpr uint32_t kHalfTx = CF::kTileBytes + (kRowTma ? CF::kRowBytes : 0);
             int* tr = trace_slot(p.P);   // NULL unless the visit order is being recorded
             int visits = 0, cur_i = -1;
             for (int n = 0; n < NT; ++n, qi.next()) {
                 const int s = n % CF::kStages;
                 const uint32_t ph = (uint32_t)(n / CF::kStages) & 1u;
-                ok = mbar_wait_poll(bar_qdo_empty(s), ph ^ 1u, wc);
+                ok = mbar_wait_poll(bar_k_done(s), ph ^ 1u, wc);   // dK of the stage's last tile read its Q
                 if (!ok) break;
                 const int q0 = qi.q_start();
                 const int qh = qi.q_head();
@@ -302,27 +327,33 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                     tr[visits * kTraceInts + 3] += 1;
                     tr[visits * kTraceInts + 5] = q0;
                 }
-                mbar_arrive_expect_tx(bar_qdo_full(s), kStageTx);
+                const int b_idx = qh / p.H;
+                mbar_arrive_expect_tx(bar_q_full(s), kHalfTx);
                 for (int x = 0; x < CF::kBoxes; ++x) {
-                    if constexpr (kStrided) {
-                        const int b_idx = qh / p.H;
-                        tma_load_rows(sQ + s * CF::kTileBytes + x * CF::kBoxBytes, &map_q, bar_qdo_full(s),
+                    if constexpr (kStrided)
+                        tma_load_rows(sQ + s * CF::kTileBytes + x * CF::kBoxBytes, &map_q, bar_q_full(s),
                                       64 * x, q0, qh - b_idx * p.H, b_idx, p.H, (p.rank4 & 1) != 0);
-                        tma_load_rows(sDO + s * CF::kTileBytes + x * CF::kBoxBytes, &map_do, bar_qdo_full(s),
+                    else
+                        tma_load_3d(sQ + s * CF::kTileBytes + x * CF::kBoxBytes, &map_q, bar_q_full(s), 64 * x, q0, qh);
+                }
+                if constexpr (kRowTma) tma_load_2d(sRow + s * 2 * CF::kRowBytes, &map_lse2, bar_q_full(s), q0, qh);
+                issued_q[s] = (int)ph;
+                // dO and the D rows: once the stage's last tile is past its dS
+                // phase and (D = 128) the dQ rows staged in its dO buffer have
+                // been reduced
+                ok = mbar_wait_poll(bar_do_empty(s), ph ^ 1u, wc);
+                if (!ok) break;
+                mbar_arrive_expect_tx(bar_do_full(s), kHalfTx);
+                for (int x = 0; x < CF::kBoxes; ++x) {
+                    if constexpr (kStrided)
+                        tma_load_rows(sDO + s * CF::kTileBytes + x * CF::kBoxBytes, &map_do, bar_do_full(s),
                                       64 * x, q0, qh - b_idx * p.H, b_idx, p.H, (p.rank4 & 8) != 0);
-                    } else {
-                        tma_load_3d(sQ + s * CF::kTileBytes + x * CF::kBoxBytes, &map_q,
-                                    bar_qdo_full(s), 64 * x, q0, qh);
-                        tma_load_3d(sDO + s * CF::kTileBytes + x * CF::kBoxBytes, &map_do,
-                                    bar_qdo_full(s), 64 * x, q0, qh);
-                    }
+                    else
+                        tma_load_3d(sDO + s * CF::kTileBytes + x * CF::kBoxBytes, &map_do, bar_do_full(s), 64 * x, q0, qh);
                 }
-                if constexpr (kRowTma) {
-                    tma_load_2d(sRow + s * 2 * CF::kRowBytes, &map_lse2, bar_qdo_full(s), q0, qh);
-                    tma_load_2d(sRow + s * 2 * CF::kRowBytes + CF::kRowBytes, &map_dvec,
-                                bar_qdo_full(s), q0, qh);
-                }
-                issued[s] = (int)ph;
+                if constexpr (kRowTma)
+                    tma_load_2d(sRow + s * 2 * CF::kRowBytes + CF::kRowBytes, &map_dvec, bar_do_full(s), q0, qh);
+                issued_do[s] = (int)ph;
             }
             if (tr) trace_put(tr, bkv, chunk_j, kt, visits, NT, p.group);
             if (!ok) {
@@ -330,8 +361,10 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 volatile int dummy = 0;
                 drain.abort_flag = &dummy;
                 mbar_wait(bar_kv, 0, drain);
-                for (int s = 0; s < CF::kStages; ++s)
-                    if (issued[s] >= 0) mbar_wait(bar_qdo_full(s), (uint32_t)issued[s], drain);
+                for (int s = 0; s < CF::kStages; ++s) {
+                    if (issued_q[s] >= 0) mbar_wait(bar_q_full(s), (uint32_t)issued_q[s], drain);
+                    if (issued_do[s] >= 0) mbar_wait(bar_do_full(s), (uint32_t)issued_do[s], drain);
+                }
             }
         } else if (warp == 1) {
             // -------------------------------------------------------- MMA
@@ -378,14 +411,13 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             auto wait_all = [&](uint32_t bar, uint32_t parity) {
                 return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc));
             };
-            const uint64_t dds0 = sdesc_sw128(sDS, CF::kBoxBytes, 1024);
             const uint64_t dk0 = sdesc_sw128(sK, CF::kBoxBytes, 1024);
             bool ok = wait_all(bar_kv, 0);
             for (int n = 0; n < NT && ok; ++n) {
                 const int s = n % CF::kStages;
                 const uint32_t ph = (uint32_t)(n / CF::kStages) & 1u;
                 const uint32_t par = (uint32_t)n & 1u;
-                ok = wait_all(bar_qdo_full(s), ph);
+                ok = wait_all(bar_q_full(s), ph);
                 if (ok && n > 0) ok = wait_all(bar_dq_free, par ^ 1u);
                 if (!ok) break;
                 tc_fence_after();
@@ -393,18 +425,23 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 const uint32_t dos = sDO + s * CF::kTileBytes;
                 mma_kmajor(tmem + CF::kColS, sK, qs);
                 commit(bar_s_full);
+                ok = wait_all(bar_do_full(s), ph);
+                if (!ok) break;
+                tc_fence_after();
                 mma_kmajor(tmem + CF::kColDP, sV, dos);
                 commit(bar_dp_full);
                 ok = wait_all(bar_p_ready, par);
                 if (!ok) break;
                 tc_fence_after();
                 mma_ts(tmem + CF::kColDV, tmem + CF::kColS, dos, n == 0);
+                commit(bar_dv_done(s));
                 ok = wait_all(bar_ds_ready, par);
                 if (!ok) break;
                 tc_fence_after();
                 // dQ tile = dS K into the S region (P^T there was consumed by
                 // dV, issued before).  A is dS^T stored [key][query] (queries
                 // contiguous, MN-major); B is the K tile (d contiguous).
+                const uint64_t dds0 = sdesc_sw128(base + ds_off(s), CF::kBoxBytes, 1024);
                 if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
@@ -424,34 +461,38 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             __all_sync(0xffffffffu, mbar_wait(bar_drain, 0, drain));
         } else if (warp == 2 && lane == 0) {
             // ---------------------------------------------------- dQ reducer
-            // For each tile: add rows 0-63 (D / 32 boxes [64 rows x 32
-            // columns] in the dS buffer) and rows 64-127 (the same boxes in
-            // the stage's dO buffer) to the fp32 accumulator; free the dS
-            // buffer, and then the stage once dK has read its Q too, as the
-            // bulk copies finish reading them.  Rows past S are skipped by the
-            // TMA; rows past the chunk end hold exact zeros (their P is
-            // masked to 0).
+            // For each tile: add rows 0-63, then rows 64-127 (D / 32 boxes
+            // [64 rows x 32 columns] each) to the fp32 accumulator; hand the
+            // stage back once dK has read its Q and (D = 128) the first half,
+            // staged in its dO buffer, has been read; then free the staging
+            // buffer.  Rows past S are skipped by the TMA; rows past the chunk
+            // end hold exact zeros (their P is masked to 0).
             tma_prefetch_desc(&map_dq);
             for (int n = 0; n < NT; ++n, qi.next()) {
                 const int s = n % CF::kStages;
                 const uint32_t par = (uint32_t)n & 1u;
                 const int q0 = qi.q_start();
+                const uint32_t src_a = CF::kDsInDo ? sDO + s * CF::kTileBytes : sStg;
+                const uint32_t src_b = CF::kDsInDo ? sStg : sStg + CF::kStgBytes / 2;
                 if (!mbar_wait_poll(bar_dqa_staged, par, wc)) break;
+                // D = 64: staging began after dq_full, so every softmax warp
+                // is past its dS phase (D rows read) and dV has read dO
+                if constexpr (!CF::kDsInDo) mbar_arrive(bar_do_empty(s));
 #pragma unroll
                 for (int b = 0; b < D / 32; ++b)
-                    tma_reduce_add_3d(&map_dq, sDS + (uint32_t)b * 8192u, 32 * b, q0, qi.q_head());
+                    tma_reduce_add_3d(&map_dq, src_a + (uint32_t)b * 8192u, 32 * b, q0, qi.q_head());
                 bulk_commit_group();
                 if (!mbar_wait_poll(bar_dqb_staged, par, wc)) break;
 #pragma unroll
                 for (int b = 0; b < D / 32; ++b)
-                    tma_reduce_add_3d(&map_dq, sDO + s * CF::kTileBytes + (uint32_t)b * 8192u, 32 * b, q0 + 64,
-                                      qi.q_head());
+                    tma_reduce_add_3d(&map_dq, src_b + (uint32_t)b * 8192u, 32 * b, q0 + 64, qi.q_head());
                 bulk_commit_group();
-                bulk_wait_read_1();
-                mbar_arrive(bar_ds_free);
+                if constexpr (CF::kDsInDo) {
+                    bulk_wait_read_1();                  // the half in the dO buffer has been read
+                    mbar_arrive(bar_do_empty(s));
+                }
                 bulk_wait_read_all();
-                if (!mbar_wait_poll(bar_k_done(s), (uint32_t)(n / CF::kStages) & 1u, wc)) break;   // dK read Q
-                mbar_arrive(bar_qdo_empty(s));
+                mbar_arrive(bar_stg_free);
             }
             bulk_wait_all();
         }
@@ -479,10 +520,10 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             const float* lse_s = reinterpret_cast<const float*>(smem + CF::kOffRow + s * 2 * CF::kRowBytes) + 32 * g;
             const float* d_s = lse_s + kBQ;
             const size_t grow = (size_t)qi.q_head() * p.S;
+            const uint32_t sph = (uint32_t)(n / CF::kStages) & 1u;   // phase of this stage's barriers
             if constexpr (kRowTma) {
-                // the rows arrived with the Q / dO tile of this stage
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(bar_qdo_full(s), (uint32_t)(n / CF::kStages) & 1u, wc));
+                // the LSE2 rows arrived with the Q tile of this stage
+                ok = __all_sync(0xffffffffu, mbar_wait(bar_q_full(s), sph, wc));
                 if (!ok) break;
             }
             ok = __all_sync(0xffffffffu, mbar_wait(bar_s_full, (uint32_t)n & 1u, wc));
@@ -534,6 +575,11 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 
             ok = __all_sync(0xffffffffu, mbar_wait(bar_dp_full, (uint32_t)n & 1u, wc));
             if (!ok) break;
+            if constexpr (kRowTma) {
+                // the D rows arrived with the dO tile (dP^T has read it already)
+                ok = __all_sync(0xffffffffu, mbar_wait(bar_do_full(s), sph, wc));
+                if (!ok) break;
+            }
             tc_fence_after();
             uint32_t pk[16];
             {
@@ -562,13 +608,14 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             // dS to shared memory as [key][query] rows, 128-byte swizzle: the
             // 16-byte chunk c of row kr sits at chunk position c ^ (kr & 7);
             // this group's 32 queries are chunks 4 (g & 1) .. +3 of atom g / 2.
-            // The buffer held the previous tile's dQ rows 0-63 until their
-            // reduction read them.
-            if (n > 0) {
-                ok = __all_sync(0xffffffffu, mbar_wait(bar_ds_free, (uint32_t)(n - 1) & 1u, wc));
+            // D = 128: the buffer is this tile's dO, once dV has read it.
+            // D = 64: the dS buffer, last read by the previous tile's dQ MMA,
+            // which finished before its dq_full.
+            if constexpr (CF::kDsInDo) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar_dv_done(s), sph, wc));
                 if (!ok) break;
             }
-            uint8_t* ds_row = smem + CF::kOffDS + (g >> 1) * CF::kBoxBytes + kr * 128;
+            uint8_t* ds_row = smem + ds_off(s) + (g >> 1) * CF::kBoxBytes + kr * 128;
 #pragma unroll
             for (int c = 0; c < 4; ++c)
                 *reinterpret_cast<uint4*>(ds_row + (((4 * (g & 1) + c) ^ (kr & 7)) << 4)) =
@@ -596,15 +643,22 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             // Stage the scaled values: box b = (kDqCols g) / 32 holds d
             // columns [32 b, 32 b + 32) for 64 rows (8 KB), 128 bytes per
             // row, 16-byte chunk c of row r at chunk position c ^ (r & 7).
-            // Rows 0-63 go to the dS buffer (the dQ MMA has read it), rows
-            // 64-127 to this tile's dO buffer (dV, issued before dQ, has read
-            // it): both at once.
+            // D = 128: rows 0-63 go to this tile's dO buffer, where dS was
+            // (the dQ MMA has read it), rows 64-127 to the staging buffer.
+            // D = 64: both halves to the staging buffer.  The staging buffer
+            // is reused once the previous tile's rows there have been read.
             {
                 const int b = (kDqCols * g) / 32;
                 const int c_first = ((kDqCols * g) % 32) / 4;
                 const bool upper = kr < 64;              // uniform over the warp
-                uint8_t* box = upper ? smem + CF::kOffDS + b * 8192 + kr * 128
-                                     : smem + CF::kOffDO + s * CF::kTileBytes + b * 8192 + (kr - 64) * 128;
+                if ((!upper || !CF::kDsInDo) && n > 0) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar_stg_free, (uint32_t)(n - 1) & 1u, wc));
+                    if (!ok) break;
+                }
+                uint8_t* box = upper ? (CF::kDsInDo ? smem + CF::kOffDO + s * CF::kTileBytes : smem + CF::kOffStg) +
+                                           b * 8192 + kr * 128
+                                     : smem + CF::kOffStg + (CF::kDsInDo ? 0 : CF::kStgBytes / 2) + b * 8192 +
+                                           (kr - 64) * 128;
 #pragma unroll
                 for (int c = 0; c < kDqCols / 4; ++c)
                     *reinterpret_cast<float4*>(box + (((c_first + c) ^ (kr & 7)) << 4)) =
