@@ -19,30 +19,34 @@
 // head of its key/value head's group, one head after the other, so dK and dV
 // collect the whole group in TMEM.
 //
-// Per query tile, on the tensor core (bf16 x bf16 -> fp32), in issue order:
-//   S^T  = K Q^T      [keys x queries]  -> TMEM S    (A = K, B = Q, K-major)
+// Per query tile n, on the tensor core (bf16 x bf16 -> fp32), in issue order:
 //   dP^T = V dO^T     [keys x queries]  -> TMEM dP   (A = V, B = dO, K-major)
 //   dV  += P^T dO     [keys x d]         A = P^T (bf16 in TMEM), B = dO (MN-major)
-//   dQ_t = dS K       [queries x d]     -> TMEM S    A = dS (smem, MN-major), B = K (MN-major)
+//   S^T  = K Q^T      of tile n + 1     -> TMEM S    (A = K, B = Q, K-major)
 //   dK  += dS^T Q     [keys x d]         A = dS^T (bf16 in TMEM), B = Q (MN-major)
-// TMEM (512 columns): S [0,128), dP [128,256), dV [256,256+D), dK after it.
-// Softmax warpgroup g (query columns 32g..32g+31) writes its bf16 P^T over
-// S columns [32g, 32g+16) and its dS^T over dP columns [32g, 32g+16) --
-// only columns it has read itself, so the warpgroups never wait on each
-// other.  The dQ tile reuses the whole S region once dV has consumed P^T
-// (tcgen05 MMAs of a CTA run in issue order); the same warps copy it out of
-// TMEM while dK runs (warp of lane quarter q, warpgroup g: queries
-// 32q..32q+31, d columns [g D/4, (g+1) D/4)) and release the region.  They
-// write the scaled fp32 tile at once as 128-byte swizzled boxes of 32
-// columns x 64 rows.  At D = 128, dS itself was written into the tile's dO
-// buffer once dV had read it; rows 0-63 of dQ go there after the dQ MMA has
-// read dS, rows 64-127 into a staging buffer of their own.  One thread adds
-// both halves to the fp32 dQ accumulator in global memory with TMA bulk
-// reduce-adds (the SM drains reductions at ~25 B/clk, so 64 KB take some
-// 2,600+ cycles), hands the stage back to the producer as soon as the
-// first half has been read and dK has read Q, and frees the staging buffer
-// after the second.  (At D = 64 dO is too small for dS: dS keeps a buffer
-// of its own and both dQ halves go to the staging buffer.)
+//   dQ_t = dS K       [queries x d]     -> TMEM dP   A = dS (smem, MN-major), B = K (MN-major)
+// (S^T of the first tile is issued before the loop.)  TMEM (512 columns):
+// S [0,128), dP [128,256), dV [256,256+D), dK after it.  Softmax warpgroup
+// g (query columns 32g..32g+31) writes its bf16 P^T over S columns
+// [32g, 32g+16) and its dS^T over dP columns [32g, 32g+16) -- only columns
+// it has read itself, so the warpgroups never wait on each other.  tcgen05
+// MMAs of a CTA run in issue order, so S^T of tile n + 1 may overwrite the
+// S columns once dV has been issued, and dQ may overwrite the dP columns
+// once dK has been issued.  The softmax warps are software-pipelined: dS of
+// tile n, then P^T of tile n + 1 (while dK and dQ of tile n run), then the
+// dQ drain of tile n -- the warp of lane quarter q, warpgroup g copies
+// queries 32q..32q+31, d columns [g D/4, (g+1) D/4) out of TMEM, releases the
+// columns for the next dP^T, and writes the scaled fp32 values as 128-byte
+// swizzled boxes of 32 columns x 64 rows.  At D = 128, dS itself was written
+// into the tile's dO buffer once dV had read it; rows 0-63 of dQ go there
+// after the dQ MMA has read dS, rows 64-127 into a staging buffer of their
+// own.  One thread adds both halves to the fp32 dQ accumulator in global
+// memory with TMA bulk reduce-adds (the SM drains reductions at ~25 B/clk,
+// sharing its memory port with the tile loads), hands the dO buffer back to
+// the producer as soon as the first half has been read, and frees the
+// staging buffer after the second; Q goes back as soon as dK has read it.
+// (At D = 64 dO is too small for dS: dS keeps a buffer of its own and both
+// dQ halves go to the staging buffer.)
 //
 // CTA layout (640 threads, five warpgroups):
 //   WG0    warp 0 TMA producer (K, V once; Q, dO, LSE2, D tiles in ring
@@ -413,19 +417,36 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             };
             const uint64_t dk0 = sdesc_sw128(sK, CF::kBoxBytes, 1024);
             bool ok = wait_all(bar_kv, 0);
+            auto issue_dq = [&](int s, uint32_t d_col) {
+                // dQ tile = dS K.  A is dS^T stored [key][query] (queries
+                // contiguous, MN-major); B is the K tile (d contiguous).
+                const uint64_t dds0 = sdesc_sw128(base + ds_off(s), CF::kBoxBytes, 1024);
+                if (elect_one()) {
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        mma_bf16_ss(tmem + d_col, dds0 + (uint32_t)kk * (2048 >> 4), dk0 + (uint32_t)kk * (2048 >> 4),
+                                    idesc_qd, kk > 0 ? 1u : 0u);
+                }
+                __syncwarp();
+            };
+            // S^T of tile n + 1 is issued right after dV of tile n (which
+            // consumes the P^T in those columns), so the softmax warps can
+            // start its P phase while dK and dQ of tile n run; dQ goes into
+            // the dP^T columns after dK has read dS^T there.
+            if (ok) ok = wait_all(bar_q_full(0), 0);
+            if (ok) {
+                tc_fence_after();
+                mma_kmajor(tmem + CF::kColS, sK, sQ);
+                commit(bar_s_full);
+            }
             for (int n = 0; n < NT && ok; ++n) {
                 const int s = n % CF::kStages;
                 const uint32_t ph = (uint32_t)(n / CF::kStages) & 1u;
                 const uint32_t par = (uint32_t)n & 1u;
-                ok = wait_all(bar_q_full(s), ph);
-                if (ok && n > 0) ok = wait_all(bar_dq_free, par ^ 1u);
-                if (!ok) break;
-                tc_fence_after();
                 const uint32_t qs = sQ + s * CF::kTileBytes;
                 const uint32_t dos = sDO + s * CF::kTileBytes;
-                mma_kmajor(tmem + CF::kColS, sK, qs);
-                commit(bar_s_full);
                 ok = wait_all(bar_do_full(s), ph);
+                if (ok && n > 0) ok = wait_all(bar_dq_free, par ^ 1u);   // dQ of tile n - 1 left the dP columns
                 if (!ok) break;
                 tc_fence_after();
                 mma_kmajor(tmem + CF::kColDP, sV, dos);
@@ -435,23 +456,21 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 tc_fence_after();
                 mma_ts(tmem + CF::kColDV, tmem + CF::kColS, dos, n == 0);
                 commit(bar_dv_done(s));
+                if (n + 1 < NT) {
+                    const int s1 = (n + 1) % CF::kStages;
+                    ok = wait_all(bar_q_full(s1), (uint32_t)((n + 1) / CF::kStages) & 1u);
+                    if (!ok) break;
+                    tc_fence_after();
+                    mma_kmajor(tmem + CF::kColS, sK, sQ + s1 * CF::kTileBytes);
+                    commit(bar_s_full);
+                }
                 ok = wait_all(bar_ds_ready, par);
                 if (!ok) break;
                 tc_fence_after();
-                // dQ tile = dS K into the S region (P^T there was consumed by
-                // dV, issued before).  A is dS^T stored [key][query] (queries
-                // contiguous, MN-major); B is the K tile (d contiguous).
-                const uint64_t dds0 = sdesc_sw128(base + ds_off(s), CF::kBoxBytes, 1024);
-                if (elect_one()) {
-#pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        mma_bf16_ss(tmem + CF::kColS, dds0 + (uint32_t)kk * (2048 >> 4), dk0 + (uint32_t)kk * (2048 >> 4),
-                                    idesc_qd, kk > 0 ? 1u : 0u);
-                }
-                __syncwarp();
-                commit(bar_dq_full);
                 mma_ts(tmem + CF::kColDK, tmem + CF::kColDP, qs, n == 0);
                 commit(bar_k_done(s));
+                issue_dq(s, CF::kColDP);
+                commit(bar_dq_full);
             }
             if (ok) commit(bar_kv_final);
             commit(bar_drain);
@@ -506,42 +525,56 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         const uint32_t tS = tmem_addr(tmem, quarter * 32, CF::kColS + 32u * g);
         const uint32_t tDP = tmem_addr(tmem, quarter * 32, CF::kColDP + 32u * g);
         constexpr int kDqCols = D / 4;                   // dQ columns this warp drains
-        const uint32_t tQ = tmem_addr(tmem, quarter * 32, CF::kColS + (uint32_t)(kDqCols * g));
+        const uint32_t tQ = tmem_addr(tmem, quarter * 32, CF::kColDP + (uint32_t)(kDqCols * g));
         const float sl2 = p.scale_log2;
         const float sc = p.scale;
         bool ok = true;
-        for (int n = 0; n < NT; ++n, qi.next()) {
-            const int s = n % CF::kStages;
-            const int q0 = qi.q_start();
-            const int qcol0 = q0 + 32 * g;               // position of this group's first query
-            const int q_valid = qi.chunk_end() - qcol0;  // columns < q_valid are real queries
-            const bool diag = p.causal && qi.i == chunk_j && qi.qt == kt;
-            const bool plain = key_ok && !diag && q_valid >= 32;
-            const float* lse_s = reinterpret_cast<const float*>(smem + CF::kOffRow + s * 2 * CF::kRowBytes) + 32 * g;
-            const float* d_s = lse_s + kBQ;
-            const size_t grow = (size_t)qi.q_head() * p.S;
-            const uint32_t sph = (uint32_t)(n / CF::kStages) & 1u;   // phase of this stage's barriers
+        // What the three phases need to know about one query tile.
+        struct TileInfo {
+            int n, s;
+            uint32_t sph;             // phase of the stage's barriers
+            int qcol0, q_valid;       // this group's first query; columns < q_valid are real
+            bool diag, plain;
+            size_t grow;              // row offset of the tile's head in LSE2 / D
+        };
+        auto info_of = [&](const QTiles& q, int n) {
+            TileInfo t;
+            t.n = n;
+            t.s = n % CF::kStages;
+            t.sph = (uint32_t)(n / CF::kStages) & 1u;
+            t.qcol0 = q.q_start() + 32 * g;
+            t.q_valid = q.chunk_end() - t.qcol0;
+            t.diag = p.causal && q.i == chunk_j && q.qt == kt;
+            t.plain = key_ok && !t.diag && t.q_valid >= 32;
+            t.grow = (size_t)q.q_head() * p.S;
+            return t;
+        };
+        auto lse_row = [&](const TileInfo& t) {
+            return reinterpret_cast<const float*>(smem + CF::kOffRow + t.s * 2 * CF::kRowBytes) + 32 * g;
+        };
+        float pv[32];   // P^T of the tile between its P phase and its dS phase
+
+        // P^T = exp2(S^T scale log2 e - LSE2), bf16 into the S columns.
+        auto p_phase = [&](const TileInfo& t) -> bool {
             if constexpr (kRowTma) {
                 // the LSE2 rows arrived with the Q tile of this stage
-                ok = __all_sync(0xffffffffu, mbar_wait(bar_q_full(s), sph, wc));
-                if (!ok) break;
+                if (!__all_sync(0xffffffffu, mbar_wait(bar_q_full(t.s), t.sph, wc))) return false;
             }
-            ok = __all_sync(0xffffffffu, mbar_wait(bar_s_full, (uint32_t)n & 1u, wc));
-            if (!ok) break;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_s_full, (uint32_t)t.n & 1u, wc))) return false;
             tc_fence_after();
-            float pv[32];
+            const float* lse_s = lse_row(t);
             {
                 uint32_t sv[32];
                 tmem_ld32(tS, sv);
                 tmem_ld_wait(sv);
-                if (plain) {
+                if (t.plain) {
 #pragma unroll
                     for (int c4 = 0; c4 < 8; ++c4) {
                         float4 l4;
                         if constexpr (kRowTma) {
                             l4 = reinterpret_cast<const float4*>(lse_s)[c4];
                         } else {
-                            const float* gp = p.lse2 + grow + qcol0 + 4 * c4;
+                            const float* gp = p.lse2 + t.grow + t.qcol0 + 4 * c4;
                             l4 = make_float4(gp[0], gp[1], gp[2], gp[3]);
                         }
                         pv[4 * c4 + 0] = ex2_approx(fmaf(__uint_as_float(sv[4 * c4 + 0]), sl2, -l4.x));
@@ -554,10 +587,10 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                     // query columns past the chunk end
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
-                        const bool valid = key_ok && c < q_valid && !(diag && qcol0 + c < kpos);
+                        const bool valid = key_ok && c < t.q_valid && !(t.diag && t.qcol0 + c < kpos);
                         float l;
                         if constexpr (kRowTma) l = lse_s[c];
-                        else l = valid ? p.lse2[grow + qcol0 + c] : 0.f;
+                        else l = valid ? p.lse2[t.grow + t.qcol0 + c] : 0.f;
                         const float e = ex2_approx(fmaf(__uint_as_float(sv[c]), sl2, -l));
                         pv[c] = valid ? e : 0.f;
                     }
@@ -572,15 +605,19 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar_p_ready);
+            return true;
+        };
 
-            ok = __all_sync(0xffffffffu, mbar_wait(bar_dp_full, (uint32_t)n & 1u, wc));
-            if (!ok) break;
+        // dS = P (dP - D): bf16 into shared memory (the dQ MMA's operand) and
+        // as dS^T into the dP columns (the dK MMA's operand).
+        auto ds_phase = [&](const TileInfo& t) -> bool {
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_dp_full, (uint32_t)t.n & 1u, wc))) return false;
             if constexpr (kRowTma) {
                 // the D rows arrived with the dO tile (dP^T has read it already)
-                ok = __all_sync(0xffffffffu, mbar_wait(bar_do_full(s), sph, wc));
-                if (!ok) break;
+                if (!__all_sync(0xffffffffu, mbar_wait(bar_do_full(t.s), t.sph, wc))) return false;
             }
             tc_fence_after();
+            const float* d_s = lse_row(t) + kBQ;
             uint32_t pk[16];
             {
                 uint32_t dp[32];
@@ -596,7 +633,7 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                         float dd[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            dd[e] = (x + e < q_valid) ? p.Dvec[grow + qcol0 + x + e] : 0.f;
+                            dd[e] = (x + e < t.q_valid) ? p.Dvec[t.grow + t.qcol0 + x + e] : 0.f;
                         d4 = make_float4(dd[0], dd[1], dd[2], dd[3]);
                     }
                     pk[2 * c4] = pack_bf16x2(pv[x] * (__uint_as_float(dp[x]) - d4.x),
@@ -612,10 +649,9 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             // D = 64: the dS buffer, last read by the previous tile's dQ MMA,
             // which finished before its dq_full.
             if constexpr (CF::kDsInDo) {
-                ok = __all_sync(0xffffffffu, mbar_wait(bar_dv_done(s), sph, wc));
-                if (!ok) break;
+                if (!__all_sync(0xffffffffu, mbar_wait(bar_dv_done(t.s), t.sph, wc))) return false;
             }
-            uint8_t* ds_row = smem + ds_off(s) + (g >> 1) * CF::kBoxBytes + kr * 128;
+            uint8_t* ds_row = smem + ds_off(t.s) + (g >> 1) * CF::kBoxBytes + kr * 128;
 #pragma unroll
             for (int c = 0; c < 4; ++c)
                 *reinterpret_cast<uint4*>(ds_row + (((4 * (g & 1) + c) ^ (kr & 7)) << 4)) =
@@ -625,10 +661,13 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar_ds_ready);
+            return true;
+        };
 
-            // dQ drain: this warp's query rows, d columns [g D/4, (g+1) D/4)
-            ok = __all_sync(0xffffffffu, mbar_wait(bar_dq_full, (uint32_t)n & 1u, wc));
-            if (!ok) break;
+        // dQ drain: this warp's query rows, d columns [g D/4, (g+1) D/4),
+        // out of TMEM and, scaled, into the staging boxes.
+        auto drain_phase = [&](const TileInfo& t) -> bool {
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_dq_full, (uint32_t)t.n & 1u, wc))) return false;
             tc_fence_after();
             uint32_t a[kDqCols];
             if constexpr (kDqCols == 32) {
@@ -639,7 +678,7 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 tmem_ld_wait16(*reinterpret_cast<uint32_t(*)[16]>(&a[0]));
             }
             tc_fence_before();
-            mbar_arrive(bar_dq_free);                    // the S region may be reused
+            mbar_arrive(bar_dq_free);                    // the dQ columns may be reused
             // Stage the scaled values: box b = (kDqCols g) / 32 holds d
             // columns [32 b, 32 b + 32) for 64 rows (8 KB), 128 bytes per
             // row, 16-byte chunk c of row r at chunk position c ^ (r & 7).
@@ -647,26 +686,46 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             // (the dQ MMA has read it), rows 64-127 to the staging buffer.
             // D = 64: both halves to the staging buffer.  The staging buffer
             // is reused once the previous tile's rows there have been read.
-            {
-                const int b = (kDqCols * g) / 32;
-                const int c_first = ((kDqCols * g) % 32) / 4;
-                const bool upper = kr < 64;              // uniform over the warp
-                if ((!upper || !CF::kDsInDo) && n > 0) {
-                    ok = __all_sync(0xffffffffu, mbar_wait(bar_stg_free, (uint32_t)(n - 1) & 1u, wc));
-                    if (!ok) break;
-                }
-                uint8_t* box = upper ? (CF::kDsInDo ? smem + CF::kOffDO + s * CF::kTileBytes : smem + CF::kOffStg) +
-                                           b * 8192 + kr * 128
-                                     : smem + CF::kOffStg + (CF::kDsInDo ? 0 : CF::kStgBytes / 2) + b * 8192 +
-                                           (kr - 64) * 128;
-#pragma unroll
-                for (int c = 0; c < kDqCols / 4; ++c)
-                    *reinterpret_cast<float4*>(box + (((c_first + c) ^ (kr & 7)) << 4)) =
-                        make_float4(__uint_as_float(a[4 * c]) * sc, __uint_as_float(a[4 * c + 1]) * sc,
-                                    __uint_as_float(a[4 * c + 2]) * sc, __uint_as_float(a[4 * c + 3]) * sc);
-                fence_proxy_async_smem();
-                mbar_arrive(upper ? bar_dqa_staged : bar_dqb_staged);
+            const int b = (kDqCols * g) / 32;
+            const int c_first = ((kDqCols * g) % 32) / 4;
+            const bool upper = kr < 64;              // uniform over the warp
+            if ((!upper || !CF::kDsInDo) && t.n > 0) {
+                if (!__all_sync(0xffffffffu, mbar_wait(bar_stg_free, (uint32_t)(t.n - 1) & 1u, wc))) return false;
             }
+            uint8_t* box = upper ? (CF::kDsInDo ? smem + CF::kOffDO + t.s * CF::kTileBytes : smem + CF::kOffStg) +
+                                       b * 8192 + kr * 128
+                                 : smem + CF::kOffStg + (CF::kDsInDo ? 0 : CF::kStgBytes / 2) + b * 8192 +
+                                       (kr - 64) * 128;
+#pragma unroll
+            for (int c = 0; c < kDqCols / 4; ++c)
+                *reinterpret_cast<float4*>(box + (((c_first + c) ^ (kr & 7)) << 4)) =
+                    make_float4(__uint_as_float(a[4 * c]) * sc, __uint_as_float(a[4 * c + 1]) * sc,
+                                __uint_as_float(a[4 * c + 2]) * sc, __uint_as_float(a[4 * c + 3]) * sc);
+            fence_proxy_async_smem();
+            mbar_arrive(upper ? bar_dqa_staged : bar_dqb_staged);
+            return true;
+        };
+
+        // Software-pipelined: tile n's dS phase, then tile n + 1's P phase
+        // (its S^T was issued right after dV of tile n), then tile n's dQ
+        // drain -- the next P phase runs while dK and dQ of this tile are on
+        // the tensor core.
+        TileInfo cur = info_of(qi, 0);
+        ok = p_phase(cur);
+        for (int n = 0; n < NT && ok; ++n) {
+            ok = ds_phase(cur);
+            if (!ok) break;
+            const bool more = n + 1 < NT;
+            TileInfo nxt = cur;
+            if (more) {
+                qi.next();
+                nxt = info_of(qi, n + 1);
+                ok = p_phase(nxt);
+                if (!ok) break;
+            }
+            ok = drain_phase(cur);
+            if (!ok) break;
+            cur = nxt;
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_kv_final, 0, wc));
         if (ok) {
