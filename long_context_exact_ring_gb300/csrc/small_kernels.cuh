@@ -18,10 +18,26 @@ namespace ra {
 //     O = (w_a O_a + w_b O_b) / (w_a + w_b),  lse = m + ln(w_a + w_b).
 // (0, -inf) is the identity; two -inf rows give (0, -inf).
 //
-// One warp per row, grid-stride over rows.  The row's LSE pair is read by
-// every lane before lane 0 writes the merged LSE, so lse_out may alias
-// lse_a (and o_out may alias o_a: each element is read, then written, by
-// the same lane).
+// One warp per row (four rows per warp and iteration when d is a multiple
+// of 4 up to 128, so every lane has eight 16-byte loads in flight before it
+// computes), grid-stride over rows.  A row's LSE pair is read by every lane
+// before lane 0 writes the merged LSE, so lse_out may alias lse_a (and o_out
+// may alias o_a: each element is read, then written, by the same lane).
+__device__ __forceinline__ void merge_weights(float la, float lb, float& ca, float& cb, float& lse)
+{
+    const float m = fmaxf(la, lb);
+    if (m == -INFINITY) {
+        ca = 0.f; cb = 0.f; lse = -INFINITY;
+        return;
+    }
+    const float wa = expf(la - m);
+    const float wb = expf(lb - m);
+    const float inv = 1.f / (wa + wb);
+    ca = wa * inv;
+    cb = wb * inv;
+    lse = m + logf(wa + wb);
+}
+
 __global__ void __launch_bounds__(256)
 merge_partials_kernel(const float* o_a, const float* lse_a, const float* __restrict__ o_b,
                       const float* lse_b, float* o_out, float* lse_out, long long rows, int d)
@@ -29,39 +45,60 @@ merge_partials_kernel(const float* o_a, const float* lse_a, const float* __restr
     const long long warp_global = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long warp_count = ((long long)gridDim.x * blockDim.x) >> 5;
     const int lane = threadIdx.x & 31;
-    const bool vec4 = (d & 3) == 0;
-    for (long long r = warp_global; r < rows; r += warp_count) {
-        const float la = lse_a[r];
-        const float lb = lse_b[r];
-        const float m = fmaxf(la, lb);
-        float wa, wb, inv;
-        if (m == -INFINITY) {
-            wa = 0.f; wb = 0.f; inv = 0.f;
-        } else {
-            wa = expf(la - m);
-            wb = expf(lb - m);
-            inv = 1.f / (wa + wb);
-        }
-        const float ca = wa * inv, cb = wb * inv;
-        const size_t base = (size_t)r * d;
-        if (vec4) {
-            const float4* a4 = reinterpret_cast<const float4*>(o_a + base);
-            const float4* b4 = reinterpret_cast<const float4*>(o_b + base);
-            float4* o4 = reinterpret_cast<float4*>(o_out + base);
-            for (int x = lane; x < (d >> 2); x += 32) {
-                const float4 a = a4[x], b = b4[x];
-                o4[x] = make_float4(ca * a.x + cb * b.x, ca * a.y + cb * b.y, ca * a.z + cb * b.z,
-                                    ca * a.w + cb * b.w);
+    if ((d & 3) == 0 && d <= 128) {
+        constexpr int R = 4;
+        const int nv = d >> 2;                      // float4 per row; lanes >= nv idle
+        const float4* a4 = reinterpret_cast<const float4*>(o_a);
+        const float4* b4 = reinterpret_cast<const float4*>(o_b);
+        float4* o4 = reinterpret_cast<float4*>(o_out);
+        for (long long r0 = warp_global * R; r0 < rows; r0 += warp_count * R) {
+            float la[R], lb[R];
+            float4 a[R], b[R];
+#pragma unroll
+            for (int k = 0; k < R; ++k) {
+                const long long r = r0 + k;
+                la[k] = lb[k] = -INFINITY;
+                a[k] = b[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (r < rows) {
+                    la[k] = lse_a[r];
+                    lb[k] = lse_b[r];
+                    if (lane < nv) {
+                        a[k] = a4[r * nv + lane];
+                        b[k] = b4[r * nv + lane];
+                    }
+                }
             }
-        } else {
-            for (int x = lane; x < d; x += 32) o_out[base + x] = ca * o_a[base + x] + cb * o_b[base + x];
+            float lo[R];
+#pragma unroll
+            for (int k = 0; k < R; ++k) {
+                float ca, cb;
+                merge_weights(la[k], lb[k], ca, cb, lo[k]);
+                const long long r = r0 + k;
+                if (r < rows && lane < nv)
+                    o4[r * nv + lane] = make_float4(ca * a[k].x + cb * b[k].x, ca * a[k].y + cb * b[k].y,
+                                                    ca * a[k].z + cb * b[k].z, ca * a[k].w + cb * b[k].w);
+            }
+            __syncwarp();
+            if (lane == 0) {
+#pragma unroll
+                for (int k = 0; k < R; ++k)
+                    if (r0 + k < rows) lse_out[r0 + k] = lo[k];
+            }
         }
+        return;
+    }
+    for (long long r = warp_global; r < rows; r += warp_count) {
+        float ca, cb, lo;
+        merge_weights(lse_a[r], lse_b[r], ca, cb, lo);
+        const size_t base = (size_t)r * d;
+        for (int x = lane; x < d; x += 32) o_out[base + x] = ca * o_a[base + x] + cb * o_b[base + x];
         __syncwarp();
-        if (lane == 0) lse_out[r] = (m == -INFINITY) ? -INFINITY : m + logf(wa + wb);
+        if (lane == 0) lse_out[r] = lo;
     }
 }
 
-// Backward preparation, one warp per row:
+// Backward preparation, one warp per row (contiguous tensors: four rows per
+// warp and iteration, all loads issued before the reductions):
 //   D_r = sum_k dO_rk * O_rk (fp32 accumulate of the bf16 inputs) and
 //   lse2_r = LSE_r * log2(e) (the exponent base the main kernel uses).
 // Row r = (b H + h) S + s of D and lse2.  kStrided: O and dO rows are
@@ -91,17 +128,68 @@ bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, RowLayout lo, const __nv_bf
         hi = bh0 - bi * H;
     }
     const size_t col = (size_t)lane * kPer;
-    for (; r < r_end; r += kStrided ? 1 : warp_count) {
-        size_t base_o, base_do;
-        if constexpr (kStrided) {
-            base_o = lo.row(bi, hi, pos) + col;
-            base_do = ldo.row(bi, hi, pos) + col;
-            if (++pos == S) {
-                pos = 0;
-                if (++hi == H) { hi = 0; ++bi; }
+    if constexpr (!kStrided) {
+        // four rows per warp and iteration: every lane has eight loads in
+        // flight before the reductions
+        constexpr int R = 4;
+        for (long long r0 = warp_global * R; r0 < rows; r0 += warp_count * R) {
+            float acc[R];
+            if constexpr (kPer == 4) {
+                uint2 a[R], b[R];
+#pragma unroll
+                for (int k = 0; k < R; ++k) {
+                    const long long rr = min(r0 + k, rows - 1);
+                    a[k] = *reinterpret_cast<const uint2*>(o + (size_t)rr * D + col);
+                    b[k] = *reinterpret_cast<const uint2*>(dO + (size_t)rr * D + col);
+                }
+#pragma unroll
+                for (int k = 0; k < R; ++k) {
+                    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[k]);
+                    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b[k]);
+                    float x = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float2 fa = __bfloat1622float2(a2[e]);
+                        const float2 fb = __bfloat1622float2(b2[e]);
+                        x = fmaf(fa.x, fb.x, x);
+                        x = fmaf(fa.y, fb.y, x);
+                    }
+                    acc[k] = x;
+                }
+            } else {
+                __nv_bfloat162 a[R], b[R];
+#pragma unroll
+                for (int k = 0; k < R; ++k) {
+                    const long long rr = min(r0 + k, rows - 1);
+                    a[k] = *reinterpret_cast<const __nv_bfloat162*>(o + (size_t)rr * D + col);
+                    b[k] = *reinterpret_cast<const __nv_bfloat162*>(dO + (size_t)rr * D + col);
+                }
+#pragma unroll
+                for (int k = 0; k < R; ++k) {
+                    const float2 fa = __bfloat1622float2(a[k]);
+                    const float2 fb = __bfloat1622float2(b[k]);
+                    acc[k] = fmaf(fa.y, fb.y, fa.x * fb.x);
+                }
             }
-        } else {
-            base_o = base_do = (size_t)r * D + col;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                for (int k = 0; k < R; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], off);
+            if (lane < R && r0 + lane < rows) {
+                float x = acc[0];
+#pragma unroll
+                for (int k = 1; k < R; ++k) if (lane == k) x = acc[k];
+                Dvec[r0 + lane] = x;
+                lse2[r0 + lane] = lse[r0 + lane] * 1.4426950408889634f;
+            }
+        }
+    } else {
+    for (; r < r_end; ++r) {   // strided: each warp walks its own run of rows
+        const size_t base_o = lo.row(bi, hi, pos) + col;
+        const size_t base_do = ldo.row(bi, hi, pos) + col;
+        if (++pos == S) {
+            pos = 0;
+            if (++hi == H) { hi = 0; ++bi; }
         }
         float acc = 0.f;
         if constexpr (kPer == 4) {
@@ -130,6 +218,7 @@ bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, RowLayout lo, const __nv_bf
             Dvec[r] = acc;
             lse2[r] = lse[r] * 1.4426950408889634f;
         }
+    }
     }
 }
 
