@@ -202,8 +202,12 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     // while its dO is still loading behind the reductions that share the
     // SM's memory port.
     auto bar_q_full = [&](int s) { return bar0 + 8u * (1 + s); };
-    auto bar_do_full = [&](int s) { return bar0 + 8u * (3 + s); };
-    auto bar_do_empty = [&](int s) { return bar0 + 8u * (19 + s); };
+    // dO arrives and is released box by box (64 d columns each): at D = 128
+    // the dQ rows staged in its first half of columns are reduced first, so
+    // the next dO's first box can load, and dP^T's first k-steps run, while
+    // the rest is still being read.  The D rows ride with box 1.
+    auto bar_do_full = [&](int s, int x) { return bar0 + 8u * (x == 0 ? 3 + s : 27 + s); };
+    auto bar_do_empty = [&](int s, int x) { return bar0 + 8u * (x == 0 ? 19 + s : 29 + s); };
     const uint32_t bar_s_full = bar0 + 8u * 5;
     const uint32_t bar_dp_full = bar0 + 8u * 6;
     const uint32_t bar_p_ready = bar0 + 8u * 7;
@@ -221,7 +225,8 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     // in the staging buffer; the stage is handed back once dK has read Q and
     // the first half has been reduced.  D = 64: both halves in the staging
     // buffer; the stage is handed back once dK has read Q.
-    const uint32_t bar_dqa_staged = bar0 + 8u * 14;  // rows 0-63 staged
+    // rows 0-63 staged by warpgroup g (d columns [g D/4, (g+1) D/4))
+    auto bar_dqa_staged = [&](int g) { return bar0 + 8u * (g == 0 ? 14u : g == 1 ? 22u : g == 2 ? 23u : 26u); };
     const uint32_t bar_dqb_staged = bar0 + 8u * 15;  // rows 64-127 staged
     const uint32_t bar_stg_free = bar0 + 8u * 16;    // the staging buffer's rows have been read
     // dV of the stage's tile has read its dO (D = 128: dS may go there).
@@ -253,8 +258,10 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         mbar_init(bar_kv, 1);
         for (int s = 0; s < CF::kStages; ++s) {
             mbar_init(bar_q_full(s), 1);
-            mbar_init(bar_do_full(s), 1);
-            mbar_init(bar_do_empty(s), 1);
+            for (int x = 0; x < 2; ++x) {
+                mbar_init(bar_do_full(s, x), 1);
+                mbar_init(bar_do_empty(s, x), 1);
+            }
             mbar_init(bar_dv_done(s), 1);
         }
         mbar_init(bar_s_full, 1);
@@ -266,7 +273,7 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         mbar_init(bar_kv_final, 1);
         mbar_init(bar_drain, 1);
         for (int s = 0; s < CF::kStages; ++s) mbar_init(bar_k_done(s), 1);
-        mbar_init(bar_dqa_staged, kSoftmaxThreads / 2);
+        for (int g = 0; g < 4; ++g) mbar_init(bar_dqa_staged(g), kSoftmaxThreads / 8);
         mbar_init(bar_dqb_staged, kSoftmaxThreads / 2);
         mbar_init(bar_stg_free, 1);
         fence_mbar_init();
@@ -308,8 +315,8 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                     tma_load_3d(sV + x * CF::kBoxBytes, &map_v, bar_kv, 64 * x, k0, bkv);
                 }
             }
-            int issued_q[CF::kStages], issued_do[CF::kStages];
-            for (int s = 0; s < CF::kStages; ++s) issued_q[s] = issued_do[s] = -1;
+            int issued_q[CF::kStages], issued_do[CF::kStages][2];
+            for (int s = 0; s < CF::kStages; ++s) issued_q[s] = issued_do[s][0] = issued_do[s][1] = -1;
             bool ok = true;
             constexpr uint32_t kHalfTx = CF::kTileBytes + (kRowTma ? CF::kRowBytes : 0);
             int* tr = trace_slot(p.P);   // NULL unless the visit order is being recorded
@@ -342,22 +349,29 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 }
                 if constexpr (kRowTma) tma_load_2d(sRow + s * 2 * CF::kRowBytes, &map_lse2, bar_q_full(s), q0, qh);
                 issued_q[s] = (int)ph;
-                // dO and the D rows: once the stage's last tile is past its dS
-                // phase and (D = 128) the dQ rows staged in its dO buffer have
-                // been reduced
-                ok = mbar_wait_poll(bar_do_empty(s), ph ^ 1u, wc);
-                if (!ok) break;
-                mbar_arrive_expect_tx(bar_do_full(s), kHalfTx);
-                for (int x = 0; x < CF::kBoxes; ++x) {
-                    if constexpr (kStrided)
-                        tma_load_rows(sDO + s * CF::kTileBytes + x * CF::kBoxBytes, &map_do, bar_do_full(s),
-                                      64 * x, q0, qh - b_idx * p.H, b_idx, p.H, (p.rank4 & 8) != 0);
-                    else
-                        tma_load_3d(sDO + s * CF::kTileBytes + x * CF::kBoxBytes, &map_do, bar_do_full(s), 64 * x, q0, qh);
+                // dO and the D rows, box by box: once the stage's last tile is
+                // past its dS phase and (D = 128) the dQ rows staged in that
+                // box have been reduced
+                for (int x = 0; x < 2 && ok; ++x) {
+                    ok = mbar_wait_poll(bar_do_empty(s, x), ph ^ 1u, wc);
+                    if (!ok) break;
+                    const bool has_box = x < CF::kBoxes;
+                    const uint32_t tx = (has_box ? CF::kBoxBytes : 0) + ((x == 1 && kRowTma) ? CF::kRowBytes : 0);
+                    if (tx) mbar_arrive_expect_tx(bar_do_full(s, x), tx);
+                    else mbar_arrive(bar_do_full(s, x));
+                    if (has_box) {
+                        if constexpr (kStrided)
+                            tma_load_rows(sDO + s * CF::kTileBytes + x * CF::kBoxBytes, &map_do, bar_do_full(s, x),
+                                          64 * x, q0, qh - b_idx * p.H, b_idx, p.H, (p.rank4 & 8) != 0);
+                        else
+                            tma_load_3d(sDO + s * CF::kTileBytes + x * CF::kBoxBytes, &map_do, bar_do_full(s, x), 64 * x,
+                                        q0, qh);
+                    }
+                    if (kRowTma && x == 1)
+                        tma_load_2d(sRow + s * 2 * CF::kRowBytes + CF::kRowBytes, &map_dvec, bar_do_full(s, 1), q0, qh);
+                    issued_do[s][x] = (int)ph;
                 }
-                if constexpr (kRowTma)
-                    tma_load_2d(sRow + s * 2 * CF::kRowBytes + CF::kRowBytes, &map_dvec, bar_do_full(s), q0, qh);
-                issued_do[s] = (int)ph;
+                if (!ok) break;
             }
             if (tr) trace_put(tr, bkv, chunk_j, kt, visits, NT, p.group);
             if (!ok) {
@@ -367,7 +381,8 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 mbar_wait(bar_kv, 0, drain);
                 for (int s = 0; s < CF::kStages; ++s) {
                     if (issued_q[s] >= 0) mbar_wait(bar_q_full(s), (uint32_t)issued_q[s], drain);
-                    if (issued_do[s] >= 0) mbar_wait(bar_do_full(s), (uint32_t)issued_do[s], drain);
+                    for (int x = 0; x < 2; ++x)
+                        if (issued_do[s][x] >= 0) mbar_wait(bar_do_full(s, x), (uint32_t)issued_do[s][x], drain);
                 }
             }
         } else if (warp == 1) {
@@ -382,12 +397,12 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             // A k-step moves a descriptor's start address (its low field,
             // address / 16) by a constant.
             // C = A(smem, K-major) * B(smem, K-major)^T over the head dim.
-            auto mma_kmajor = [&](uint32_t d_tmem, uint32_t sa, uint32_t sb) {
+            auto mma_kmajor = [&](uint32_t d_tmem, uint32_t sa, uint32_t sb, int kk0 = 0, int kk1 = D / 16) {
                 const uint64_t da = sdesc_sw128(sa, 16, 1024);
                 const uint64_t db = sdesc_sw128(sb, 16, 1024);
                 if (elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
+                    for (int kk = kk0; kk < kk1; ++kk) {
                         const uint32_t off16 = ((kk >> 2) * CF::kBoxBytes + (kk & 3) * 32) >> 4;
                         mma_bf16_ss(d_tmem, da + off16, db + off16, idesc_kq, kk > 0 ? 1u : 0u);
                     }
@@ -445,11 +460,17 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 const uint32_t par = (uint32_t)n & 1u;
                 const uint32_t qs = sQ + s * CF::kTileBytes;
                 const uint32_t dos = sDO + s * CF::kTileBytes;
-                ok = wait_all(bar_do_full(s), ph);
+                ok = wait_all(bar_do_full(s, 0), ph);
                 if (ok && n > 0) ok = wait_all(bar_dq_free, par ^ 1u);   // dQ of tile n - 1 left the dP columns
                 if (!ok) break;
                 tc_fence_after();
-                mma_kmajor(tmem + CF::kColDP, sV, dos);
+                mma_kmajor(tmem + CF::kColDP, sV, dos, 0, 4);             // d columns 0-63 (dO box 0)
+                if constexpr (CF::kBoxes == 2) {
+                    ok = wait_all(bar_do_full(s, 1), ph);
+                    if (!ok) break;
+                    tc_fence_after();
+                    mma_kmajor(tmem + CF::kColDP, sV, dos, 4, 8);         // d columns 64-127 (dO box 1)
+                }
                 commit(bar_dp_full);
                 ok = wait_all(bar_p_ready, par);
                 if (!ok) break;
@@ -493,22 +514,39 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 const int q0 = qi.q_start();
                 const uint32_t src_a = CF::kDsInDo ? sDO + s * CF::kTileBytes : sStg;
                 const uint32_t src_b = CF::kDsInDo ? sStg : sStg + CF::kStgBytes / 2;
-                if (!mbar_wait_poll(bar_dqa_staged, par, wc)) break;
-                // D = 64: staging began after dq_full, so every softmax warp
-                // is past its dS phase (D rows read) and dV has read dO
-                if constexpr (!CF::kDsInDo) mbar_arrive(bar_do_empty(s));
+                bool okr = true;
+                if constexpr (CF::kDsInDo) {
+                    // rows 0-63, box by box as each warpgroup has staged its
+                    // columns; boxes 0-1 lie in dO box 0, boxes 2-3 in dO box 1
+                    for (int b = 0; b < 4 && okr; ++b) {
+                        okr = mbar_wait_poll(bar_dqa_staged(b), par, wc);
+                        if (!okr) break;
+                        tma_reduce_add_3d(&map_dq, src_a + (uint32_t)b * 8192u, 32 * b, q0, qi.q_head());
+                        bulk_commit_group();
+                    }
+                    if (!okr) break;
+                    bulk_wait_read_n<2>();              // dQ boxes 0-1 read: dO box 0 may be reloaded
+                    mbar_arrive(bar_do_empty(s, 0));
+                } else {
+                    for (int g = 0; g < 4 && okr; ++g) okr = mbar_wait_poll(bar_dqa_staged(g), par, wc);
+                    if (!okr) break;
+                    // D = 64: staging began after dq_full, so every softmax
+                    // warp is past its dS phase (D rows read) and dV has read dO
+                    mbar_arrive(bar_do_empty(s, 0));
+                    mbar_arrive(bar_do_empty(s, 1));
 #pragma unroll
-                for (int b = 0; b < D / 32; ++b)
-                    tma_reduce_add_3d(&map_dq, src_a + (uint32_t)b * 8192u, 32 * b, q0, qi.q_head());
-                bulk_commit_group();
+                    for (int b = 0; b < D / 32; ++b)
+                        tma_reduce_add_3d(&map_dq, src_a + (uint32_t)b * 8192u, 32 * b, q0, qi.q_head());
+                    bulk_commit_group();
+                }
                 if (!mbar_wait_poll(bar_dqb_staged, par, wc)) break;
 #pragma unroll
                 for (int b = 0; b < D / 32; ++b)
                     tma_reduce_add_3d(&map_dq, src_b + (uint32_t)b * 8192u, 32 * b, q0 + 64, qi.q_head());
                 bulk_commit_group();
                 if constexpr (CF::kDsInDo) {
-                    bulk_wait_read_1();                  // the half in the dO buffer has been read
-                    mbar_arrive(bar_do_empty(s));
+                    bulk_wait_read_1();                  // dQ boxes 2-3 read: dO box 1 may be reloaded
+                    mbar_arrive(bar_do_empty(s, 1));
                 }
                 bulk_wait_read_all();
                 mbar_arrive(bar_stg_free);
@@ -614,7 +652,7 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             if (!__all_sync(0xffffffffu, mbar_wait(bar_dp_full, (uint32_t)t.n & 1u, wc))) return false;
             if constexpr (kRowTma) {
                 // the D rows arrived with the dO tile (dP^T has read it already)
-                if (!__all_sync(0xffffffffu, mbar_wait(bar_do_full(t.s), t.sph, wc))) return false;
+                if (!__all_sync(0xffffffffu, mbar_wait(bar_do_full(t.s, 1), t.sph, wc))) return false;
             }
             tc_fence_after();
             const float* d_s = lse_row(t) + kBQ;
@@ -685,11 +723,13 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             // D = 128: rows 0-63 go to this tile's dO buffer, where dS was
             // (the dQ MMA has read it), rows 64-127 to the staging buffer.
             // D = 64: both halves to the staging buffer.  The staging buffer
-            // is reused once the previous tile's rows there have been read.
+            // is reused once the previous tile's rows there have been read;
+            // every warp waits for that, so no staging barrier can run a
+            // phase ahead of the reducer.
             const int b = (kDqCols * g) / 32;
             const int c_first = ((kDqCols * g) % 32) / 4;
             const bool upper = kr < 64;              // uniform over the warp
-            if ((!upper || !CF::kDsInDo) && t.n > 0) {
+            if (t.n > 0) {
                 if (!__all_sync(0xffffffffu, mbar_wait(bar_stg_free, (uint32_t)(t.n - 1) & 1u, wc))) return false;
             }
             uint8_t* box = upper ? (CF::kDsInDo ? smem + CF::kOffDO + t.s * CF::kTileBytes : smem + CF::kOffStg) +
@@ -702,7 +742,7 @@ ring_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                     make_float4(__uint_as_float(a[4 * c]) * sc, __uint_as_float(a[4 * c + 1]) * sc,
                                 __uint_as_float(a[4 * c + 2]) * sc, __uint_as_float(a[4 * c + 3]) * sc);
             fence_proxy_async_smem();
-            mbar_arrive(upper ? bar_dqa_staged : bar_dqb_staged);
+            mbar_arrive(upper ? bar_dqa_staged(g) : bar_dqb_staged);
             return true;
         };
 
