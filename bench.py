@@ -56,12 +56,12 @@ METRIC = "attention TFLOP/s and tokens/s at 1 GB300 (fwd, fwd+bwd); % of dense B
 # source: once the source changes the counters no longer describe the
 # kernel and the line reports them as null.
 KERNEL_COUNTERS = {
-    "ring_fwd_kernel": {"traffic": None, "tensor_pipe_pct": None,
+    "ring_fwd_kernel": {"traffic": (432312320 + 125444352) * 8, "tensor_pipe_pct": 72.28,
                         "sources": ("fwd_kernel.cuh", "sm103_ptx.cuh", "layout.cuh", "trace.cuh"),
-                        "sha1": None},
-    "ring_bwd_kernel": {"traffic": None, "tensor_pipe_pct": None,
+                        "sha1": "580be25a384e17b2db2344b2e56b64d92b96bb89"},
+    "ring_bwd_kernel": {"traffic": (1770757000 + 1036869000) * 8, "tensor_pipe_pct": 54.64,
                         "sources": ("bwd_kernel.cuh", "sm103_ptx.cuh", "layout.cuh", "trace.cuh"),
-                        "sha1": None},
+                        "sha1": "1ffc5b9eff44a1559e97c5a6e8b61da4115837f0"},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
