@@ -89,15 +89,16 @@ def test_bwd_repeatable_workspace_reuse(ra):
         assert (x.float() - y.float()).abs().max().item() <= 1e-2
 
 
-@pytest.mark.parametrize("d", [128, 64])
-def test_bwd_causal_s4096_whole_tensor(ra, d):
+@pytest.mark.parametrize("d,P,causal", [(128, 4, True), (64, 4, True), (128, 8, False)])
+def test_bwd_s4096_whole_tensor(ra, d, P, causal):
     # the 128K fwd+bwd recipe at S = 4096 (P = 4, C = 1024: eight key tiles
     # per chunk), every element of dQ, dK and dV against the plain derivative;
     # d = 64 takes the other shared-memory plan (dS in a buffer of its own,
-    # the whole dQ tile in the staging buffer)
-    inp = workloads.make(workloads.FWDBWD_CAUSAL_128K, B=1, H=2, S=4096, d=d, P=4, seed=44)
+    # the whole dQ tile in the staging buffer); the non-causal case with
+    # P = 8 has every key tile meet all eight query chunks
+    inp = workloads.make(workloads.FWDBWD_CAUSAL_128K, B=1, H=2, S=4096, d=d, P=P, causal=causal, seed=44)
     q, k, v, do, o, lse, dq, dk, dv = _fwd_bwd(ra, inp)
-    dq_r, dk_r, dv_r, _, _ = oracle.bwd(f64(q), f64(k), f64(v), f64(do), True, inp["scale"])
+    dq_r, dk_r, dv_r, _, _ = oracle.bwd(f64(q), f64(k), f64(v), f64(do), causal, inp["scale"])
     assert_grad_max(f64(dq), dq_r, "dQ")
     assert_grad_max(f64(dk), dk_r, "dK")
     assert_grad_max(f64(dv), dv_r, "dV")
