@@ -97,8 +97,10 @@ merge_partials_kernel(const float* o_a, const float* lse_a, const float* __restr
     }
 }
 
-// Backward preparation, one warp per row (contiguous tensors: four rows per
-// warp and iteration, all loads issued before the reductions):
+// Backward preparation (contiguous tensors: each lane loads 8 bf16 -- 16
+// bytes -- of a row of O and of dO, D / 8 lanes per row, four rows' loads
+// per lane in flight before the reductions; strided tensors: one warp per
+// row):
 //   D_r = sum_k dO_rk * O_rk (fp32 accumulate of the bf16 inputs) and
 //   lse2_r = LSE_r * log2(e) (the exponent base the main kernel uses).
 // Row r = (b H + h) S + s of D and lse2.  kStrided: O and dO rows are
@@ -112,113 +114,85 @@ bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, RowLayout lo, const __nv_bf
     const long long warp_global = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long warp_count = ((long long)gridDim.x * blockDim.x) >> 5;
     const int lane = threadIdx.x & 31;
-    constexpr int kPer = D / 32;   // elements per lane (2 or 4)
-    // Strided: each warp takes a contiguous run of rows and steps (position,
-    // head, batch) along it, so the only divisions are at its start.
-    // Contiguous: warps stride over rows.
+    // Strided: each warp takes a contiguous run of rows; contiguous: warps
+    // stride over rows.  Both give each lane 8 bf16 (16 bytes) of a row of O
+    // and of dO, D / 8 lanes per row, and sum in the same order, so D comes
+    // out bit-identical for any row layout.
     const long long per = kStrided ? (rows + warp_count - 1) / warp_count : 0;
-    long long r = kStrided ? warp_global * per : warp_global;
+    const long long r = kStrided ? warp_global * per : warp_global;
     const long long r_end = kStrided ? min(rows, r + per) : rows;
-    int pos = 0, bi = 0, hi = 0;
-    if constexpr (kStrided) {
-        if (r >= r_end) return;
-        const int bh0 = (int)r / S;          // rows < 2^31 (checked by the host)
-        pos = (int)r - bh0 * S;
-        bi = bh0 / H;
-        hi = bh0 - bi * H;
-    }
-    const size_t col = (size_t)lane * kPer;
     if constexpr (!kStrided) {
-        // four rows per warp and iteration: every lane has eight loads in
-        // flight before the reductions
-        constexpr int R = 4;
+        // lanes take 8 bf16 (16 bytes) of a row: kLpr lanes per row, kRpl
+        // rows per warp-wide load, four loads per tensor in flight per lane
+        constexpr int kLpr = D / 8, kRpl = 32 / kLpr, R = 4 * kRpl;
+        const int g = lane / kLpr;
+        const size_t c8 = (size_t)(lane % kLpr) * 8;
         for (long long r0 = warp_global * R; r0 < rows; r0 += warp_count * R) {
-            float acc[R];
-            if constexpr (kPer == 4) {
-                uint2 a[R], b[R];
+            uint4 a[4], b[4];
 #pragma unroll
-                for (int k = 0; k < R; ++k) {
-                    const long long rr = min(r0 + k, rows - 1);
-                    a[k] = *reinterpret_cast<const uint2*>(o + (size_t)rr * D + col);
-                    b[k] = *reinterpret_cast<const uint2*>(dO + (size_t)rr * D + col);
+            for (int i = 0; i < 4; ++i) {
+                const long long rr = min(r0 + i * kRpl + g, rows - 1);
+                a[i] = *reinterpret_cast<const uint4*>(o + (size_t)rr * D + c8);
+                b[i] = *reinterpret_cast<const uint4*>(dO + (size_t)rr * D + c8);
+            }
+            float acc[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[i]);
+                const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b[i]);
+                float x = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 fa = __bfloat1622float2(a2[e]);
+                    const float2 fb = __bfloat1622float2(b2[e]);
+                    x = fmaf(fa.x, fb.x, x);
+                    x = fmaf(fa.y, fb.y, x);
                 }
-#pragma unroll
-                for (int k = 0; k < R; ++k) {
-                    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[k]);
-                    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b[k]);
-                    float x = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float2 fa = __bfloat1622float2(a2[e]);
-                        const float2 fb = __bfloat1622float2(b2[e]);
-                        x = fmaf(fa.x, fb.x, x);
-                        x = fmaf(fa.y, fb.y, x);
-                    }
-                    acc[k] = x;
-                }
-            } else {
-                __nv_bfloat162 a[R], b[R];
-#pragma unroll
-                for (int k = 0; k < R; ++k) {
-                    const long long rr = min(r0 + k, rows - 1);
-                    a[k] = *reinterpret_cast<const __nv_bfloat162*>(o + (size_t)rr * D + col);
-                    b[k] = *reinterpret_cast<const __nv_bfloat162*>(dO + (size_t)rr * D + col);
-                }
-#pragma unroll
-                for (int k = 0; k < R; ++k) {
-                    const float2 fa = __bfloat1622float2(a[k]);
-                    const float2 fb = __bfloat1622float2(b[k]);
-                    acc[k] = fmaf(fa.y, fb.y, fa.x * fb.x);
-                }
+                acc[i] = x;
             }
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
+            for (int off = kLpr / 2; off > 0; off >>= 1)
 #pragma unroll
-                for (int k = 0; k < R; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], off);
-            if (lane < R && r0 + lane < rows) {
-                float x = acc[0];
+                for (int i = 0; i < 4; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
+            if (lane % kLpr == 0) {
 #pragma unroll
-                for (int k = 1; k < R; ++k) if (lane == k) x = acc[k];
-                Dvec[r0 + lane] = x;
-                lse2[r0 + lane] = lse[r0 + lane] * 1.4426950408889634f;
+                for (int i = 0; i < 4; ++i) {
+                    const long long rr = r0 + i * kRpl + g;
+                    if (rr < rows) {
+                        Dvec[rr] = acc[i];
+                        lse2[rr] = lse[rr] * 1.4426950408889634f;
+                    }
+                }
             }
         }
     } else {
-    for (; r < r_end; ++r) {   // strided: each warp walks its own run of rows
-        const size_t base_o = lo.row(bi, hi, pos) + col;
-        const size_t base_do = ldo.row(bi, hi, pos) + col;
-        if (++pos == S) {
-            pos = 0;
-            if (++hi == H) { hi = 0; ++bi; }
-        }
-        float acc = 0.f;
-        if constexpr (kPer == 4) {
-            const uint2 a = *reinterpret_cast<const uint2*>(o + base_o);
-            const uint2 b = *reinterpret_cast<const uint2*>(dO + base_do);
+        constexpr int kLpr = D / 8, kRpl = 32 / kLpr;
+        const int g = lane / kLpr;
+        const size_t c8 = (size_t)(lane % kLpr) * 8;
+        for (long long r0 = r; r0 < r_end; r0 += kRpl) {
+            const long long rr = min(r0 + g, r_end - 1);
+            const int bh = (int)(rr / S);   // rows < 2^31 (checked by the host)
+            const int ps = (int)(rr - (long long)bh * S);
+            const int bq = bh / H, hq = bh - bq * H;
+            const uint4 a = *reinterpret_cast<const uint4*>(o + lo.row(bq, hq, ps) + c8);
+            const uint4 b = *reinterpret_cast<const uint4*>(dO + ldo.row(bq, hq, ps) + c8);
             const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
             const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+            float x = 0.f;
 #pragma unroll
-            for (int x = 0; x < 2; ++x) {
-                const float2 fa = __bfloat1622float2(a2[x]);
-                const float2 fb = __bfloat1622float2(b2[x]);
-                acc = fmaf(fa.x, fb.x, acc);
-                acc = fmaf(fa.y, fb.y, acc);
+            for (int e = 0; e < 4; ++e) {
+                const float2 fa = __bfloat1622float2(a2[e]);
+                const float2 fb = __bfloat1622float2(b2[e]);
+                x = fmaf(fa.x, fb.x, x);
+                x = fmaf(fa.y, fb.y, x);
             }
-        } else {
-            const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + base_o);
-            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(dO + base_do);
-            const float2 fa = __bfloat1622float2(a);
-            const float2 fb = __bfloat1622float2(b);
-            acc = fmaf(fa.x, fb.x, acc);
-            acc = fmaf(fa.y, fb.y, acc);
-        }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) {
-            Dvec[r] = acc;
-            lse2[r] = lse[r] * 1.4426950408889634f;
+            for (int off = kLpr / 2; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+            if (lane % kLpr == 0 && r0 + g < r_end) {
+                Dvec[r0 + g] = x;
+                lse2[r0 + g] = lse[r0 + g] * 1.4426950408889634f;
+            }
         }
-    }
     }
 }
 
