@@ -75,6 +75,8 @@ def parse_args():
     ap.add_argument("--workload", default=workloads.FWDBWD_CAUSAL_128K.name,
                     choices=[w.name for w in workloads.ALL])
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-groups", type=int, default=4,
+                    help="head groups per end-to-end step (each with its own copies; 1 = whole-step copies)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ring-emulation", action="store_true",
@@ -426,7 +428,8 @@ def main():
         # link's first transfer after a pause in copy traffic measured 11-200
         # GB/s on this part, against ~210 GB/s back to back.
         H_kv = inp.get("H_kv", H)
-        G = 4 if B == 1 and H % 4 == 0 and H_kv % 4 == 0 else 1   # head slices are contiguous at B = 1
+        G = args.e2e_groups if B == 1 and H % args.e2e_groups == 0 and H_kv % args.e2e_groups == 0 else 1
+        # (head slices are contiguous only at B = 1)
         hq, hkv = H // G, H_kv // G
 
         def part(t, g, nh):
